@@ -1,0 +1,202 @@
+/*
+ * clo.h -- C ABI of libclo, the GB300 (sm_103a) decode-attention hot path of
+ * CPU-light KV-cache offloading.
+ *
+ * The operations follow "CLO: CPU-Light KVCache Offloading" (section 2 and
+ * section 4): per-head similarity thresholds (Eqs. 7-9), the fused head-wise
+ * approximate-cache lookup with GQA aggregation (Eq. 10) and query-label
+ * update, and the hybrid attention kernel that reads the top-k Cache Buffer
+ * and the full-length Persistent Cache directly.  A plain paged decode
+ * attention serves the many-request case of "Neo: Saving GPU Memory Crisis
+ * with CPU Offloading for Online LLM Inference" (method details: paged KV
+ * cache, one decode attention launch per iteration) and "FastDecode" (R-Part
+ * attention over per-request KV).  The attention itself is
+ * softmax(q K^T / sqrt(d_head)) V as written in "KVPR: Efficient LLM
+ * Inference With I/O-Aware KV Cache Partial Recomputation", section A3.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous in the layouts stated per call.  fp16 data is IEEE binary16
+ *    (clo_half holds the bit pattern).  The library never allocates or frees
+ *    device memory; scratch space is caller-provided ("workspace").
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *    return after the launches are enqueued.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns CLO_ERR_INVALID_ARG (or CLO_ERR_UNSUPPORTED for a shape
+ *    this build does not implement, CLO_ERR_WORKSPACE for a short workspace)
+ *    and launches nothing.  A failed launch returns CLO_ERR_CUDA.
+ *  - Data-dependent errors (an index, block-table entry, context length or
+ *    persistent-head id out of range) are detected on the device: the kernel
+ *    ORs a CLO_FLAG_* bit into *err_flag (a caller-zeroed int32 in device
+ *    memory; may be NULL), skips the bad rows, and writes zeros (lse = -inf)
+ *    for the affected query heads.  The caller copies err_flag back after the
+ *    stream synchronises and maps it with clo_check_error_flag().  No kernel
+ *    traps.
+ *  - Query head h belongs to KV head h / G with G = Hq / Hkv (contiguous
+ *    grouping).  d (head dimension) must be 128 in this build.
+ *  - No C++ exception crosses this interface.  There is no global mutable
+ *    state besides cached device attributes, so independent calls on
+ *    different streams may run concurrently provided they do not share
+ *    output or workspace buffers.
+ */
+#ifndef CLO_H_
+#define CLO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t clo_half; /* IEEE binary16 bit pattern */
+
+typedef enum clo_status {
+    CLO_OK = 0,
+    CLO_ERR_INVALID_ARG = 1,
+    CLO_ERR_UNSUPPORTED = 2,
+    CLO_ERR_CUDA = 3,
+    CLO_ERR_BAD_INDEX = 4,
+    CLO_ERR_WORKSPACE = 5
+} clo_status;
+
+/* Bits a kernel ORs into *err_flag. */
+#define CLO_FLAG_BAD_INDEX 0x1   /* Cache Buffer index or block-table entry out of range */
+#define CLO_FLAG_BAD_PERSIST 0x2 /* persist_ids entry out of range or repeated */
+#define CLO_FLAG_BAD_CTX 0x4     /* a context length < 0 or > max_blocks*block_size */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* clo_status_string(clo_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int clo_version(void);
+
+/* Maps an err_flag value copied back to the host to a status: CLO_OK when
+ * zero, CLO_ERR_BAD_INDEX when any CLO_FLAG_* bit is set. */
+clo_status clo_check_error_flag(int32_t host_err_flag);
+
+/*
+ * clo_thresholds -- per-KV-head similarity thresholds, CLO Eqs. 7-9:
+ *     theta* = arccos(eta), lambda = s^n, theta = lambda*theta* + (1-lambda)*pi,
+ *     tau = cos(theta).
+ * s:    [n_kv * group] fp32 importance scores of the query heads (device).
+ *       KV head g uses the mean of s[g*group .. g*group+group-1]; with
+ *       group = 1 the map is elementwise.
+ * tau:  [n_kv] fp32 output (device).
+ * eta:  global similarity bound, in [-1, 1] (the page uses 0.8).
+ * n_exp: importance exponent n >= 0 (the page uses 3).
+ * Computed in fp32 with the CUDA math library (acosf, powf, cosf).
+ */
+clo_status clo_thresholds(const float* s, int n_kv, int group, float eta,
+                          float n_exp, float* tau, cudaStream_t stream);
+
+/*
+ * clo_lookup_update -- fused head-wise approximate-cache lookup and query-label
+ * update (CLO section 2 "head-wise approximate cache" and "fused cache lookup
+ * + query label update kernel"; Eq. 10; section 3 Fig. 7).  One launch reads
+ * the incoming queries and the stored labels once:
+ *     c_h   = q_h . l_h / (|q_h| |l_h|)            (0 if either norm is 0)
+ *     sim_g = sum_{h in g} w_h c_h / sum_{h in g} w_h   (plain mean if the
+ *             weights of the group sum to 0)                        Eq. 10
+ *     hit_g = sim_g >= tau_g
+ * On a miss the G labels of the group are overwritten with the G current
+ * queries (bit copies) and the head is flagged 1; a hit leaves them (flag 0);
+ * a persistent KV head is not cached (flag 2, labels untouched).
+ * q:          [B][Hq][d] fp16 (device, read).
+ * labels:     [B][Hq][d] fp16 (device, read and updated in place).
+ * w_q:        [Hq] fp32 importance weights of the query heads.
+ * tau_kv:     [Hkv] fp32 thresholds (e.g. from clo_thresholds).
+ * persist_mask: [Hkv] uint8, nonzero = persistent; may be NULL (none).
+ * flag:       [B][Hkv] uint8 output.      sim: [B][Hkv] fp32 output.
+ * miss_list:  [B*Hkv] int32 output: b*Hkv+g of every miss, ascending.
+ * miss_count: [1] int32 output: number of misses.
+ * Requires Hq % Hkv == 0, G = Hq/Hkv <= 8, d == 128, 0 <= B*Hkv <= 65536.
+ */
+clo_status clo_lookup_update(const clo_half* q, clo_half* labels,
+                             const float* w_q, const float* tau_kv,
+                             const uint8_t* persist_mask, int B, int Hq,
+                             int Hkv, int d, uint8_t* flag, float* sim,
+                             int32_t* miss_list, int32_t* miss_count,
+                             cudaStream_t stream);
+
+/* Optional tuning and instrumentation for the attention calls (may be NULL). */
+typedef struct clo_attn_opts {
+    int num_ctas;         /* CTAs of the main kernel; 0 = one per SM */
+    cudaEvent_t ev_begin; /* if non-NULL, recorded on `stream` right before the main kernel */
+    cudaEvent_t ev_end;   /* if non-NULL, recorded right after the main kernel */
+} clo_attn_opts;
+
+/*
+ * Workspace bytes clo_hybrid_decode_attn needs for these sizes when run with
+ * num_ctas CTAs (0 = one per SM of the current device).  Returns 0 for
+ * invalid sizes.  The workspace holds split-KV partial results; it needs no
+ * initialisation and may be reused by later calls on the same stream.
+ */
+size_t clo_hybrid_workspace_size(int B, int Hq, int Hkv, int d, int num_ctas);
+
+/*
+ * clo_hybrid_decode_attn -- GQA decode attention that reads the top-k Cache
+ * Buffer and the Persistent Cache in place (CLO section 2 "hybrid attention
+ * kernel", section 3 Fig. 9), with no gather into a unified buffer.
+ * For each batch row b and KV head g the attended token set is
+ *   - all T rows of Persistent Cache slot j if persist_ids[j] == g, else
+ *   - the k Cache Buffer rows idx[b][g][0..k-1] of head g.
+ * For every query head h of the group:
+ *   o_h = sum_t softmax_t(scale * q_h . K_t) V_t,  lse_h = log sum_t exp(scale * q_h . K_t).
+ * Split-KV over all SMs with a log-sum-exp merge; fp16 inputs, fp32
+ * accumulation, fp16 output rounded to nearest.
+ * q:           [B][Hq][d] fp16.
+ * cbK, cbV:    [B][Hkv][C][d] fp16 Cache Buffer (slots of persistent heads unused).
+ * idx:         [B][Hkv][k] int32 rows in [0, C); any order, duplicates allowed.
+ * pK, pV:      [B][Np][T][d] fp16 Persistent Cache; may be NULL when Np == 0.
+ * persist_ids: [Np] int32 distinct KV heads in [0, Hkv); may be NULL when Np == 0.
+ * out:         [B][Hq][d] fp16 output.    lse: [B][Hq] fp32 output or NULL.
+ * workspace:   >= clo_hybrid_workspace_size(B, Hq, Hkv, d, num_ctas) bytes,
+ *              16-byte aligned.
+ * Requires k >= 1 unless every KV head is persistent, T >= 1 when Np > 0,
+ * k <= C, 0 <= Np <= Hkv, G <= 8, d == 128.
+ */
+clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
+                                  const clo_half* cbV, const int32_t* idx,
+                                  int k, int C, const clo_half* pK,
+                                  const clo_half* pV,
+                                  const int32_t* persist_ids, int Np, int T,
+                                  int B, int Hq, int Hkv, int d, float scale,
+                                  clo_half* out, float* lse, void* workspace,
+                                  size_t ws_bytes, int32_t* err_flag,
+                                  const clo_attn_opts* opts,
+                                  cudaStream_t stream);
+
+/* Workspace bytes clo_paged_decode_attn needs (same rules as above). */
+size_t clo_paged_workspace_size(int B, int Hq, int Hkv, int d, int num_ctas);
+
+/*
+ * clo_paged_decode_attn -- dense decode attention over a paged KV cache, one
+ * query per request (NEO GPU/CPU paged attention; FastDecode R-Part).
+ * Token t < ctx_len[r] of request r is row t % block_size of block
+ * block_table[r][t / block_size].
+ * q:           [B][Hq][d] fp16.
+ * kc, vc:      [num_blocks][Hkv][block_size][d] fp16 block pool.
+ * block_table: [B][max_blocks] int32 entries in [0, num_blocks).
+ * ctx_len:     [B] int32 in [0, max_blocks*block_size]; 0 gives zeros.
+ * out, lse, workspace, err_flag, opts: as for clo_hybrid_decode_attn.
+ * Requires block_size == 16, G <= 8, d == 128, B <= 4096,
+ * B*Hkv*max_blocks < 2^31.
+ */
+clo_status clo_paged_decode_attn(const clo_half* q, const clo_half* kc,
+                                 const clo_half* vc,
+                                 const int32_t* block_table, int max_blocks,
+                                 const int32_t* ctx_len, int num_blocks, int B,
+                                 int Hq, int Hkv, int d, int block_size,
+                                 float scale, clo_half* out, float* lse,
+                                 void* workspace, size_t ws_bytes,
+                                 int32_t* err_flag, const clo_attn_opts* opts,
+                                 cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CLO_H_ */

@@ -1,0 +1,269 @@
+"""Python binding of libclo (include/clo.h): argument marshalling only.
+
+Every function here checks the torch tensors it is given (device, dtype,
+contiguity, shapes), passes their device pointers and the CUDA stream to the
+C ABI of ``libclo.so`` and raises ``CloError`` on a non-OK status.  All
+computation happens in the library's CUDA kernels; there is no CPU path.  If
+the library has not been built, the first call raises ``CloError``.
+
+Torch is used for device memory, streams and events only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libclo.so")
+
+CLO_OK = 0
+CLO_ERR_INVALID_ARG = 1
+CLO_ERR_UNSUPPORTED = 2
+CLO_ERR_CUDA = 3
+CLO_ERR_BAD_INDEX = 4
+CLO_ERR_WORKSPACE = 5
+
+FLAG_BAD_INDEX = 0x1
+FLAG_BAD_PERSIST = 0x2
+FLAG_BAD_CTX = 0x4
+
+HEAD_DIM = 128
+
+
+class CloError(RuntimeError):
+    """A libclo call returned a non-OK status (or the library is missing)."""
+
+    def __init__(self, msg: str, status: Optional[int] = None):
+        super().__init__(msg)
+        self.status = status
+
+
+class AttnOpts(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int), ("ev_begin", ctypes.c_void_p),
+                ("ev_end", ctypes.c_void_p)]
+
+
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "clo_status_string": ([_I], ctypes.c_char_p),
+    "clo_version": ([], _I),
+    "clo_check_error_flag": ([ctypes.c_int32], _I),
+    "clo_thresholds": ([_P, _I, _I, _F, _F, _P, _P], _I),
+    "clo_lookup_update": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "clo_hybrid_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
+    "clo_hybrid_decode_attn": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                _F, _P, _P, _P, _SZ, _P, _P, _P], _I),
+    "clo_paged_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
+    "clo_paged_decode_attn": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                               _P, _SZ, _P, _P, _P], _I),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libclo.so (raises CloError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise CloError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m offloaded_kv_decode_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().clo_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().clo_version())
+
+
+def check_error_flag(host_value: int) -> int:
+    return int(lib().clo_check_error_flag(int(host_value)))
+
+
+def _check(status: int, what: str):
+    if status != CLO_OK:
+        raise CloError(f"{what}: {status_string(status)}", status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype, ndim=None, optional=False) -> int:
+    if t is None:
+        if optional:
+            return 0
+        raise CloError(f"{name} is required", CLO_ERR_INVALID_ARG)
+    if not t.is_cuda:
+        raise CloError(f"{name} must be a CUDA tensor", CLO_ERR_INVALID_ARG)
+    if t.dtype != dtype:
+        raise CloError(f"{name} must be {dtype}, got {t.dtype}", CLO_ERR_INVALID_ARG)
+    if not t.is_contiguous():
+        raise CloError(f"{name} must be contiguous", CLO_ERR_INVALID_ARG)
+    if ndim is not None and t.dim() != ndim:
+        raise CloError(f"{name} must have {ndim} dims, got {tuple(t.shape)}", CLO_ERR_INVALID_ARG)
+    return t.data_ptr()
+
+
+def _events(events) -> tuple:
+    if events is None:
+        return 0, 0
+    b, e = events
+    return int(b.cuda_event), int(e.cuda_event)
+
+
+def _opts(num_ctas: int, events) -> Optional[AttnOpts]:
+    if not num_ctas and events is None:
+        return None
+    eb, ee = _events(events)
+    return AttnOpts(int(num_ctas), eb or None, ee or None)
+
+
+# ---------------------------------------------------------------- thresholds
+
+def clo_thresholds(s: torch.Tensor, tau: torch.Tensor, group: int = 1, eta: float = 0.8,
+                   n_exp: float = 3.0, stream=None) -> torch.Tensor:
+    """tau[g] = cos(lambda*arccos(eta) + (1-lambda)*pi), lambda = mean(s of group g)^n."""
+    ps = _dev(s, "s", torch.float32)
+    pt = _dev(tau, "tau", torch.float32)
+    n_kv = tau.numel()
+    if s.numel() != n_kv * group:
+        raise CloError("s must hold tau.numel()*group scores", CLO_ERR_INVALID_ARG)
+    _check(lib().clo_thresholds(ps, n_kv, group, eta, n_exp, pt, _stream(stream)),
+           "clo_thresholds")
+    return tau
+
+
+# ---------------------------------------------------------------- lookup
+
+def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
+                      tau_kv: torch.Tensor, persist_mask: Optional[torch.Tensor],
+                      flag: torch.Tensor, sim: torch.Tensor, miss_list: torch.Tensor,
+                      miss_count: torch.Tensor, stream=None):
+    """Fused head-wise cache lookup + Eq. 10 + label update (labels updated in place)."""
+    pq = _dev(q, "q", torch.float16, 3)
+    pl = _dev(labels, "labels", torch.float16, 3)
+    if labels.shape != q.shape:
+        raise CloError("labels must match q", CLO_ERR_INVALID_ARG)
+    B, Hq, d = q.shape
+    Hkv = tau_kv.numel()
+    pw = _dev(w_q, "w_q", torch.float32)
+    pt = _dev(tau_kv, "tau_kv", torch.float32)
+    pm = _dev(persist_mask, "persist_mask", torch.uint8, optional=True)
+    pf = _dev(flag, "flag", torch.uint8)
+    psim = _dev(sim, "sim", torch.float32)
+    pml = _dev(miss_list, "miss_list", torch.int32)
+    pmc = _dev(miss_count, "miss_count", torch.int32)
+    if w_q.numel() != Hq or flag.numel() != B * Hkv or sim.numel() != B * Hkv or \
+            miss_list.numel() < B * Hkv or miss_count.numel() < 1 or \
+            (persist_mask is not None and persist_mask.numel() != Hkv):
+        raise CloError("lookup buffer sizes do not match q / tau_kv", CLO_ERR_INVALID_ARG)
+    _check(lib().clo_lookup_update(pq, pl, pw, pt, pm, B, Hq, Hkv, d, pf, psim, pml, pmc,
+                                   _stream(stream)), "clo_lookup_update")
+
+
+# ---------------------------------------------------------------- attention
+
+def clo_hybrid_workspace_size(B: int, Hq: int, Hkv: int, d: int = HEAD_DIM,
+                              num_ctas: int = 0) -> int:
+    return int(lib().clo_hybrid_workspace_size(B, Hq, Hkv, d, num_ctas))
+
+
+def clo_paged_workspace_size(B: int, Hq: int, Hkv: int, d: int = HEAD_DIM,
+                             num_ctas: int = 0) -> int:
+    return int(lib().clo_paged_workspace_size(B, Hq, Hkv, d, num_ctas))
+
+
+def clo_hybrid_decode_attn(q: torch.Tensor, cbK: Optional[torch.Tensor],
+                           cbV: Optional[torch.Tensor], idx: Optional[torch.Tensor],
+                           pK: Optional[torch.Tensor], pV: Optional[torch.Tensor],
+                           persist_ids: Optional[torch.Tensor], out: torch.Tensor,
+                           workspace: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                           err_flag: Optional[torch.Tensor] = None,
+                           scale: Optional[float] = None, num_ctas: int = 0,
+                           events: Optional[Sequence] = None, stream=None):
+    """Hybrid Cache Buffer / Persistent Cache GQA decode attention.
+
+    q [B][Hq][d]; cbK/cbV [B][Hkv][C][d]; idx [B][Hkv][k] int32; pK/pV
+    [B][Np][T][d]; persist_ids [Np] int32; out [B][Hq][d] fp16; lse [B][Hq]
+    fp32 (optional); workspace: a CUDA uint8 tensor of at least
+    clo_hybrid_workspace_size(...) bytes.
+    """
+    pq = _dev(q, "q", torch.float16, 3)
+    B, Hq, d = q.shape
+    Np = 0 if persist_ids is None else persist_ids.numel()
+    if cbK is not None:
+        Hkv, C = cbK.shape[1], cbK.shape[2]
+        k = idx.shape[2] if idx is not None else 0
+    else:
+        Hkv, C, k = Np, 0, 0
+    T = pK.shape[2] if (pK is not None and Np > 0) else 0
+    pcbk = _dev(cbK, "cbK", torch.float16, 4, optional=True)
+    pcbv = _dev(cbV, "cbV", torch.float16, 4, optional=True)
+    pidx = _dev(idx, "idx", torch.int32, 3, optional=True)
+    ppk = _dev(pK, "pK", torch.float16, 4, optional=True) if Np > 0 else 0
+    ppv = _dev(pV, "pV", torch.float16, 4, optional=True) if Np > 0 else 0
+    ppid = _dev(persist_ids, "persist_ids", torch.int32, optional=True) if Np > 0 else 0
+    pout = _dev(out, "out", torch.float16, 3)
+    plse = _dev(lse, "lse", torch.float32, optional=True)
+    pws = _dev(workspace, "workspace", torch.uint8)
+    perr = _dev(err_flag, "err_flag", torch.int32, optional=True)
+    if out.shape != q.shape or (lse is not None and lse.numel() != B * Hq):
+        raise CloError("out / lse shapes do not match q", CLO_ERR_INVALID_ARG)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_hybrid_decode_attn(
+        pq, pcbk, pcbv, pidx, k, C, ppk, ppv, ppid, Np, T, B, Hq, Hkv, d, float(scale),
+        pout, plse, pws, workspace.numel(), perr,
+        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "clo_hybrid_decode_attn")
+
+
+def clo_paged_decode_attn(q: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor,
+                          block_table: torch.Tensor, ctx_len: torch.Tensor, out: torch.Tensor,
+                          workspace: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                          err_flag: Optional[torch.Tensor] = None,
+                          scale: Optional[float] = None, num_ctas: int = 0,
+                          events: Optional[Sequence] = None, stream=None):
+    """Paged decode attention: q [B][Hq][d]; kc/vc [num_blocks][Hkv][16][d];
+    block_table [B][max_blocks] int32; ctx_len [B] int32."""
+    pq = _dev(q, "q", torch.float16, 3)
+    B, Hq, d = q.shape
+    pk = _dev(kc, "kc", torch.float16, 4)
+    pv = _dev(vc, "vc", torch.float16, 4)
+    num_blocks, Hkv, bs = kc.shape[0], kc.shape[1], kc.shape[2]
+    pbt = _dev(block_table, "block_table", torch.int32, 2)
+    pcl = _dev(ctx_len, "ctx_len", torch.int32)
+    pout = _dev(out, "out", torch.float16, 3)
+    plse = _dev(lse, "lse", torch.float32, optional=True)
+    pws = _dev(workspace, "workspace", torch.uint8)
+    perr = _dev(err_flag, "err_flag", torch.int32, optional=True)
+    if out.shape != q.shape or ctx_len.numel() != B or block_table.shape[0] != B or \
+            vc.shape != kc.shape:
+        raise CloError("paged buffer shapes do not match", CLO_ERR_INVALID_ARG)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_paged_decode_attn(
+        pq, pk, pv, pbt, block_table.shape[1], pcl, num_blocks, B, Hq, Hkv, d, bs,
+        float(scale), pout, plse, pws, workspace.numel(), perr,
+        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "clo_paged_decode_attn")

@@ -1,0 +1,20 @@
+// clo_api.cu -- status helpers of the libclo C ABI (host only).
+#include "clo.h"
+
+extern "C" const char* clo_status_string(clo_status s) {
+    switch (s) {
+        case CLO_OK: return "CLO_OK";
+        case CLO_ERR_INVALID_ARG: return "CLO_ERR_INVALID_ARG";
+        case CLO_ERR_UNSUPPORTED: return "CLO_ERR_UNSUPPORTED";
+        case CLO_ERR_CUDA: return "CLO_ERR_CUDA";
+        case CLO_ERR_BAD_INDEX: return "CLO_ERR_BAD_INDEX";
+        case CLO_ERR_WORKSPACE: return "CLO_ERR_WORKSPACE";
+    }
+    return "CLO_ERR_UNKNOWN";
+}
+
+extern "C" int clo_version(void) { return 100; }
+
+extern "C" clo_status clo_check_error_flag(int32_t host_err_flag) {
+    return host_err_flag == 0 ? CLO_OK : CLO_ERR_BAD_INDEX;
+}

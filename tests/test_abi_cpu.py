@@ -1,0 +1,126 @@
+"""libclo loads, exports every declared entry point, and rejects bad arguments
+on the host before launching anything (CPU only: no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import offloaded_kv_decode_gb300 as clo
+from offloaded_kv_decode_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "clo.h")
+FAKE = 1 << 20  # aligned non-null stand-in pointer: never dereferenced on these paths
+
+
+@pytest.fixture(scope="module")
+def L():
+    libbuild.build()
+    return clo.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(clo_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) == 9, names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in clo.h but not exported"
+
+
+def test_status_helpers(L):
+    assert clo.status_string(0) == "CLO_OK"
+    assert clo.status_string(4) == "CLO_ERR_BAD_INDEX"
+    assert clo.version() >= 100
+    assert clo.check_error_flag(0) == clo.CLO_OK
+    assert clo.check_error_flag(clo.FLAG_BAD_INDEX | clo.FLAG_BAD_PERSIST) == clo.CLO_ERR_BAD_INDEX
+
+
+def test_workspace_size_formula(L):
+    # (CTAs + B*Hkv) partial slots of G*(128 floats + 1 lse), each array padded to 256 B.
+    def expect(B, Hq, Hkv, C):
+        slots = C + B * Hkv
+        G = Hq // Hkv
+        o = slots * G * 128 * 4
+        l = slots * G * 4
+        return -(-o // 256) * 256 + -(-l // 256) * 256
+    for (B, Hq, Hkv, C) in [(1, 32, 8, 152), (8, 32, 8, 152), (16, 40, 8, 7), (256, 32, 32, 152)]:
+        assert clo.clo_hybrid_workspace_size(B, Hq, Hkv, 128, C) == expect(B, Hq, Hkv, C)
+        assert clo.clo_paged_workspace_size(B, Hq, Hkv, 128, C) == expect(B, Hq, Hkv, C)
+    assert clo.clo_hybrid_workspace_size(1, 30, 8, 128, 4) == 0   # Hq % Hkv
+    assert clo.clo_hybrid_workspace_size(1, 32, 8, 64, 4) == 0    # d != 128
+    assert clo.clo_hybrid_workspace_size(1, 72, 8, 128, 4) == 0   # G > 8
+
+
+def test_thresholds_rejects(L):
+    assert L.clo_thresholds(None, 4, 1, 0.8, 3.0, FAKE, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_thresholds(FAKE, 4, 0, 0.8, 3.0, FAKE, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_thresholds(FAKE, 4, 1, 1.5, 3.0, FAKE, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_thresholds(FAKE, 0, 1, 0.8, 3.0, FAKE, None) == clo.CLO_OK  # empty: no launch
+
+
+def _lookup(L, q=FAKE, B=1, Hq=32, Hkv=8, d=128, miss=FAKE):
+    return L.clo_lookup_update(q, FAKE, FAKE, FAKE, None, B, Hq, Hkv, d, FAKE, FAKE, miss,
+                               FAKE, None)
+
+
+def test_lookup_rejects(L):
+    assert _lookup(L, q=None) == clo.CLO_ERR_INVALID_ARG
+    assert _lookup(L, miss=None) == clo.CLO_ERR_INVALID_ARG
+    assert _lookup(L, Hq=30) == clo.CLO_ERR_INVALID_ARG
+    assert _lookup(L, B=-1) == clo.CLO_ERR_INVALID_ARG
+    assert _lookup(L, q=FAKE + 2) == clo.CLO_ERR_INVALID_ARG     # misaligned fp16 tensor
+    assert _lookup(L, d=64) == clo.CLO_ERR_UNSUPPORTED
+    assert _lookup(L, Hq=72) == clo.CLO_ERR_UNSUPPORTED           # G = 9
+    assert _lookup(L, B=9000) == clo.CLO_ERR_UNSUPPORTED          # > 65536 groups
+
+
+def _hybrid(L, k=10, C=100, Np=2, T=50, B=1, Hq=32, Hkv=8, d=128, scale=0.088, ws=FAKE,
+            wsb=1 << 30, idx=FAKE, pK=FAKE, pid=FAKE):
+    return L.clo_hybrid_decode_attn(FAKE, FAKE, FAKE, idx, k, C, pK, FAKE, pid, Np, T, B, Hq,
+                                    Hkv, d, scale, FAKE, None, ws, wsb, None, None, None)
+
+
+def test_hybrid_rejects(L):
+    assert _hybrid(L, k=0) == clo.CLO_ERR_INVALID_ARG          # Cache Buffer heads need k >= 1
+    assert _hybrid(L, k=101) == clo.CLO_ERR_INVALID_ARG        # k > C
+    assert _hybrid(L, Np=9) == clo.CLO_ERR_INVALID_ARG         # Np > Hkv
+    assert _hybrid(L, T=0) == clo.CLO_ERR_INVALID_ARG          # persistent heads need T >= 1
+    assert _hybrid(L, idx=None) == clo.CLO_ERR_INVALID_ARG
+    assert _hybrid(L, pK=None) == clo.CLO_ERR_INVALID_ARG
+    assert _hybrid(L, pid=None) == clo.CLO_ERR_INVALID_ARG
+    assert _hybrid(L, scale=0.0) == clo.CLO_ERR_INVALID_ARG
+    assert _hybrid(L, scale=float("nan")) == clo.CLO_ERR_INVALID_ARG
+    assert _hybrid(L, d=96) == clo.CLO_ERR_UNSUPPORTED
+    assert _hybrid(L, Hq=80, Hkv=8) == clo.CLO_ERR_UNSUPPORTED  # G = 10
+    assert _hybrid(L, B=0) == clo.CLO_OK                        # empty batch: nothing to do
+    # All heads persistent: no Cache Buffer pointers needed, k may be 0.
+    assert L.clo_hybrid_decode_attn(FAKE, None, None, None, 0, 0, FAKE, FAKE, FAKE, 8, 5, 0,
+                                    32, 8, 128, 0.1, FAKE, None, FAKE, 1 << 20, None, None,
+                                    None) == clo.CLO_OK
+
+
+def _paged(L, B=4, Hq=32, Hkv=32, d=128, bs=16, mb=8, nb=64, bt=FAKE):
+    return L.clo_paged_decode_attn(FAKE, FAKE, FAKE, bt, mb, FAKE, nb, B, Hq, Hkv, d, bs, 0.088,
+                                   FAKE, None, FAKE, 1 << 30, None, None, None)
+
+
+def test_paged_rejects(L):
+    assert _paged(L, bt=None) == clo.CLO_ERR_INVALID_ARG
+    assert _paged(L, mb=0) == clo.CLO_ERR_INVALID_ARG
+    assert _paged(L, bs=32) == clo.CLO_ERR_UNSUPPORTED
+    assert _paged(L, B=5000) == clo.CLO_ERR_UNSUPPORTED
+    assert _paged(L, B=4096, Hkv=64, Hq=64, mb=1 << 14) == clo.CLO_ERR_UNSUPPORTED  # tile ids overflow
+    assert _paged(L, B=0) == clo.CLO_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(clo, "_lib", None)
+    monkeypatch.setattr(clo, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(clo.CloError):
+        clo.lib()
