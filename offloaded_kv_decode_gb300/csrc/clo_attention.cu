@@ -37,8 +37,6 @@
 //    is ORed into err_flag and the affected outputs are written as zeros.
 #include <math.h>
 
-#include <mutex>
-
 #include "clo_device.cuh"
 
 namespace clo {
@@ -53,10 +51,12 @@ constexpr int OSTRIDE = D + 4;  // padded merge-area row (floats): conflict-free
 constexpr int ATTN_WARPS = 8;
 constexpr int ATTN_STAGES = 3;
 constexpr int ATTN_THREADS = ATTN_WARPS * 32;
-constexpr int MERGE_THREADS = 1024;
+constexpr int MERGE_THREADS = 512;
 constexpr int MAX_HKV_HYBRID = 64;
 constexpr int MAX_PAGED_B = 4096;
+constexpr int MAX_ROWS = 1 << 24;  // rows per head: row offsets stay 32-bit
 constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int MERGE_SMEM_LIMIT = 96 * 1024;
 
 // One token set: batch row (or request) b, KV head kv.
 struct Seg {
@@ -82,9 +82,13 @@ struct AttnOut {
 };
 
 // ---------------------------------------------------------------- hybrid geometry
-// Segments are ordered (b, slot): slots [0, Np) are the persistent heads in
-// persist_ids order (T tokens each), slots [Np, Hkv) the remaining KV heads in
-// ascending order (k indexed Cache Buffer rows each).
+// The tile stream has two parts, each cut evenly over all CTAs: part 0 holds
+// every Persistent Cache segment (ordered b, slot; T contiguous rows each),
+// part 1 every Cache Buffer segment (ordered b, slot; k indexed rows each).
+// Each CTA thus streams the same share of contiguous and of scattered rows,
+// so no SM is left with only the slower scattered reads.  Slots [0, Np) are
+// the persistent heads in persist_ids order, slots [Np, Hkv) the remaining
+// KV heads in ascending order.
 struct HybridGeo {
     const clo_half* cbK;
     const clo_half* cbV;
@@ -94,17 +98,23 @@ struct HybridGeo {
     const int32_t* persist_ids;
     int k, C, Np, T, B, Hkv;
     int tp, tc;             // tiles of a persistent / Cache Buffer segment
-    long long per_b;        // tiles per batch row
+    long long n0;           // tiles in part 0 (B * Np * tp)
+    long long n1;           // tiles in part 1 (B * (Hkv - Np) * tc)
 
-    // Shared scratch: [0] = ids valid flag, [1 .. Hkv] slot -> KV head.
-    static size_t smem_ints(int Hkv_, int /*B*/) { return static_cast<size_t>(Hkv_) + 4; }
+    static constexpr int kParts = 2;
+    // Shared scratch: [0] = ids valid flag, [1 .. Hkv] slot -> KV head,
+    // [1 + Hkv .. 1 + 2 Hkv) staged persist_ids.
+    static size_t smem_ints(int Hkv_, int /*B*/) { return 2 * static_cast<size_t>(Hkv_) + 4; }
 
     __device__ void cta_init(int* sm, int32_t* err_flag, bool report) const {
+        // sm[1 + Hkv + j] stages persist_ids so thread 0 does not wait on Np loads in turn.
+        if (static_cast<int>(threadIdx.x) < Np) sm[1 + Hkv + threadIdx.x] = persist_ids[threadIdx.x];
+        __syncthreads();
         if (threadIdx.x == 0) {
             unsigned long long used = 0ull;
             int ok = 1;
             for (int j = 0; j < Np; ++j) {
-                const int g = persist_ids[j];
+                const int g = sm[1 + Hkv + j];
                 if (g < 0 || g >= Hkv || ((used >> g) & 1ull)) {
                     ok = 0;
                     sm[1 + j] = 0;
@@ -122,51 +132,83 @@ struct HybridGeo {
             if (!ok && report) report_error(err_flag, CLO_FLAG_BAD_PERSIST);
         }
     }
-    __device__ long long num_tiles(const int*) const { return per_b * B; }
+    // Segment boundaries do not depend on device data.
+    static constexpr bool kStaticLayout = true;
+    __device__ long long part_begin(int p, const int*) const { return p == 0 ? 0 : n0; }
+    __device__ long long part_tiles(int p, const int*) const { return p == 0 ? n0 : n1; }
+    __device__ long long num_tiles(const int*) const { return n0 + n1; }
     __device__ int seg_of(long long t, const int*) const {
-        const int b = static_cast<int>(t / per_b);
-        const long long r = t - per_b * b;
-        const long long np_tiles = static_cast<long long>(Np) * tp;
-        const int slot = r < np_tiles ? static_cast<int>(r / tp)
-                                      : Np + static_cast<int>((r - np_tiles) / tc);
-        return b * Hkv + slot;
+        if (t < n0) {
+            const long long per_b = static_cast<long long>(Np) * tp;
+            const int b = static_cast<int>(t / per_b);
+            const int slot = static_cast<int>((t - per_b * b) / tp);
+            return b * Np + slot;
+        }
+        const long long t1 = t - n0;
+        const int nc = Hkv - Np;
+        const long long per_b = static_cast<long long>(nc) * tc;
+        const int b = static_cast<int>(t1 / per_b);
+        const int j = static_cast<int>((t1 - per_b * b) / tc);
+        return B * Np + b * nc + j;
+    }
+    __device__ long long segment_first(int s) const {
+        return s < B * Np ? static_cast<long long>(s) * tp
+                          : n0 + static_cast<long long>(s - B * Np) * tc;
     }
     __device__ Seg segment(int s, const int* sm) const {
         Seg g;
-        g.b = s / Hkv;
-        const int slot = s - g.b * Hkv;
+        int slot;
+        if (s < B * Np) {
+            g.b = s / Np;
+            slot = s - g.b * Np;
+            g.n_tok = T;
+            g.ntiles = tp;
+            g.first = static_cast<long long>(s) * tp;
+            g.slot = slot;
+        } else {
+            const int nc = Hkv - Np;
+            const int s1 = s - B * Np;
+            g.b = s1 / nc;
+            const int j = s1 - g.b * nc;
+            slot = Np + j;
+            g.n_tok = k;
+            g.ntiles = tc;
+            g.first = n0 + static_cast<long long>(s1) * tc;
+            g.slot = -1;
+        }
         g.kv = sm[1 + slot];
-        const bool pers = slot < Np;
-        g.slot = pers ? slot : -1;
-        g.n_tok = pers ? T : k;
-        g.ntiles = pers ? tp : tc;
-        g.first = per_b * g.b + (pers ? static_cast<long long>(slot) * tp
-                                      : static_cast<long long>(Np) * tp +
-                                            static_cast<long long>(slot - Np) * tc);
         return g;
     }
     __device__ bool all_bad(const int* sm) const { return sm[0] == 0; }
-    // Row `row` (0..15) of tile `tile_in` of segment g: element offset of the
-    // row from the returned base pointers; in_range / ok as described.
-    __device__ void row(const Seg& g, int tile_in, int r, const int* sm, const clo_half*& bk,
-                        const clo_half*& bv, long long& off, bool& in_range, bool& ok) const {
+    // The indirection of row r (0..15) of a tile: its Cache Buffer index
+    // (0 for persistent rows and rows past the end).  Issued one pipeline
+    // step before the row is copied so its latency overlaps the math.
+    __device__ int row_load(const Seg& g, int tile_in, int r) const {
+        const int tok = tile_in * TILE + r;
+        if (g.slot >= 0 || tok >= g.n_tok) return 0;
+        return __ldg(idx + (static_cast<long long>(g.b) * Hkv + g.kv) * k + tok);
+    }
+    // Row r of tile `tile_in` of segment g: the segment's K/V base (uniform over
+    // the tile) and the row's element offset from it (< 2^31: C, T <= 2^24);
+    // in_range = the token exists, ok = its address is valid.
+    __device__ void row(const Seg& g, int tile_in, int r, int raw, const int* sm,
+                        const clo_half*& bk, const clo_half*& bv, int& roff, bool& in_range,
+                        bool& ok) const {
         const int tok = tile_in * TILE + r;
         in_range = tok < g.n_tok;
         if (g.slot >= 0) {
-            bk = pK;
-            bv = pV;
-            off = (static_cast<long long>(g.b) * Np + g.slot) * T + tok;
+            const long long base = (static_cast<long long>(g.b) * Np + g.slot) * T * D;
+            bk = pK + base;
+            bv = pV + base;
+            roff = tok * D;
             ok = sm[0] != 0;
         } else {
-            bk = cbK;
-            bv = cbV;
-            const long long hb = static_cast<long long>(g.b) * Hkv + g.kv;
-            int iv = 0;
-            if (in_range) iv = __ldg(idx + hb * k + tok);
-            ok = (sm[0] != 0) && iv >= 0 && iv < C;
-            off = hb * C + (ok ? iv : 0);
+            const long long base = (static_cast<long long>(g.b) * Hkv + g.kv) * C * D;
+            bk = cbK + base;
+            bv = cbV + base;
+            ok = (sm[0] != 0) && raw >= 0 && raw < C;
+            roff = (ok ? raw : 0) * D;
         }
-        off *= D;
     }
 };
 
@@ -233,6 +275,10 @@ struct PagedGeo {
             prefix[r + 1] = run;
         }
     }
+    static constexpr int kParts = 1;
+    static constexpr bool kStaticLayout = false;  // depends on ctx_len
+    __device__ long long part_begin(int, const int*) const { return 0; }
+    __device__ long long part_tiles(int, const int* sm) const { return sm[B]; }
     __device__ long long num_tiles(const int* sm) const { return sm[B]; }
     // Request owning tile t: the last r with prefix[r] <= t (skips empty requests).
     __device__ int request_of(long long t, const int* sm) const {
@@ -248,6 +294,7 @@ struct PagedGeo {
         const int tr = (sm[r + 1] - sm[r]) / Hkv;
         return r * Hkv + static_cast<int>((t - sm[r]) / tr);
     }
+    __device__ long long segment_first(int) const { return 0; }  // unused: layout is dynamic
     __device__ Seg segment(int s, const int* sm) const {
         Seg g;
         g.b = s / Hkv;
@@ -260,45 +307,83 @@ struct PagedGeo {
         return g;
     }
     __device__ bool all_bad(const int*) const { return false; }
-    __device__ void row(const Seg& g, int tile_in, int r, const int*, const clo_half*& bk,
-                        const clo_half*& bv, long long& off, bool& in_range, bool& ok) const {
-        bk = kc;
-        bv = vc;
-        in_range = tile_in * TILE + r < g.n_tok;
-        const int blk = __ldg(block_table + static_cast<long long>(g.b) * max_blocks + tile_in);
+    // The block holding tile `tile_in` (the same for all 16 rows).
+    __device__ int row_load(const Seg& g, int tile_in, int /*r*/) const {
+        return __ldg(block_table + static_cast<long long>(g.b) * max_blocks + tile_in);
+    }
+    __device__ void row(const Seg& g, int tile_in, int r, int blk, const int*,
+                        const clo_half*& bk, const clo_half*& bv, int& roff, bool& in_range,
+                        bool& ok) const {
         ok = blk >= 0 && blk < num_blocks;
-        off = ((static_cast<long long>(ok ? blk : 0) * Hkv + g.kv) * TILE + r) * D;
+        const long long base = (static_cast<long long>(ok ? blk : 0) * Hkv + g.kv) * TILE * D;
+        bk = kc + base;
+        bv = vc + base;
+        in_range = tile_in * TILE + r < g.n_tok;
+        roff = r * D;
     }
 };
 
 // ---------------------------------------------------------------- tile copy
+// Producer-side position in the segment order.  A warp's tiles increase, so
+// the segment of the next tile is found by stepping forward from the last one
+// (no per-tile division).
+struct Cursor {
+    int s;
+    Seg sg;
+};
+
+template <class Geo>
+__device__ __forceinline__ void cursor_init(const Geo& geo, const int* gsm, long long t, Cursor& c) {
+    c.s = geo.seg_of(t, gsm);
+    c.sg = geo.segment(c.s, gsm);
+}
+
+template <class Geo>
+__device__ __forceinline__ void cursor_seek(const Geo& geo, const int* gsm, long long t, Cursor& c) {
+    while (t >= c.sg.first + c.sg.ntiles) c.sg = geo.segment(++c.s, gsm);
+}
+
+// A tile whose segment is located and whose row indirection load is in
+// flight; the copies are issued one pipeline step later.
+struct Pending {
+    Seg sg;
+    int tile_in;
+    int raw;
+};
+
+template <class Geo>
+__device__ __forceinline__ void prefetch_tile(const Geo& geo, const int* gsm, long long t, int lane,
+                                              Cursor& cur, Pending& pd) {
+    cursor_seek(geo, gsm, t, cur);
+    pd.sg = cur.sg;
+    pd.tile_in = static_cast<int>(t - cur.sg.first);
+    pd.raw = geo.row_load(pd.sg, pd.tile_in, lane & 15);
+}
+
 // Issues the cp.async copies of one tile (16 K rows + 16 V rows) into a ring
 // stage and records its row masks (bits 0-15 valid rows, 16-31 bad rows).
 template <class Geo>
-__device__ __forceinline__ void issue_tile(const Geo& geo, const int* gsm, long long t,
-                                           uint32_t stage, uint32_t* mask_slot, int lane) {
-    const int s = geo.seg_of(t, gsm);
-    const Seg sg = geo.segment(s, gsm);
-    const int tile_in = static_cast<int>(t - sg.first);
+__device__ __forceinline__ void issue_tile(const Geo& geo, const int* gsm, const Pending& pd,
+                                           uint32_t stage, uint32_t* mask_slot, int lane,
+                                           uint64_t policy) {
     const clo_half* bk;
     const clo_half* bv;
-    long long off;
+    int roff;
     bool in_range, ok;
-    geo.row(sg, tile_in, lane & 15, gsm, bk, bv, off, in_range, ok);
+    geo.row(pd.sg, pd.tile_in, lane & 15, pd.raw, gsm, bk, bv, roff, in_range, ok);
     const unsigned valid = __ballot_sync(FULL_MASK, in_range && ok) & 0xffffu;
     const unsigned bad = __ballot_sync(FULL_MASK, in_range && !ok) & 0xffffu;
     if (lane == 0) *mask_slot = valid | (bad << 16);
     const int chunk = lane & 15;
+    const uint32_t dst0 = stage + (lane >> 4) * ROW_BYTES;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = (lane >> 4) + 2 * i;
-        const long long ro = __shfl_sync(FULL_MASK, off, r);
+        const int ro = __shfl_sync(FULL_MASK, roff, r) + chunk * 8;
         const bool v = (valid >> r) & 1u;
-        const uint32_t dst = stage + r * ROW_BYTES + ((chunk ^ (r & 7)) << 4);
-        const clo_half* sk = v ? bk + ro + chunk * 8 : bk;
-        const clo_half* sv = v ? bv + ro + chunk * 8 : bv;
-        cp_async_16(dst, sk, v ? 16 : 0);
-        cp_async_16(dst + KV_TILE_BYTES, sv, v ? 16 : 0);
+        const uint32_t dst = dst0 + 2 * i * ROW_BYTES + ((chunk ^ (r & 7)) << 4);
+        cp_async_16_hint(dst, bk + (v ? ro : 0), v ? 16 : 0, policy);
+        cp_async_16_hint(dst + KV_TILE_BYTES, bv + (v ? ro : 0), v ? 16 : 0, policy);
     }
 }
 
@@ -324,16 +409,21 @@ __device__ __forceinline__ void compute_tile(uint32_t st, uint32_t valid,
                                              const uint32_t (&qb)[8][2], float sl2,
                                              WarpState& w, int lane) {
     const uint32_t Ks = st, Vs = st + KV_TILE_BYTES;
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // Two accumulators over alternating k-steps halve the mma dependency chain.
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
     const int arow = lane & 15;
     const int ahi = lane >> 4;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        uint32_t a[4];
+    for (int kk = 0; kk < 8; kk += 2) {
+        uint32_t a[4], a2[4];
         const int chunk = 2 * kk + ahi;
         ldmatrix_x4(a, Ks + arow * ROW_BYTES + ((chunk ^ (arow & 7)) << 4));
+        ldmatrix_x4(a2, Ks + arow * ROW_BYTES + (((chunk + 2) ^ (arow & 7)) << 4));
         mma_16816(s, a, qb[kk][0], qb[kk][1]);
+        mma_16816(s2, a2, qb[kk + 1][0], qb[kk + 1][1]);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] += s2[j];
     const int r0 = lane >> 2;
     const bool v0 = (valid >> r0) & 1u;
     const bool v1 = (valid >> (r0 + 8)) & 1u;
@@ -357,12 +447,14 @@ __device__ __forceinline__ void compute_tile(uint32_t st, uint32_t valid,
     w.l1 = fmaf(w.l1, al1, p1 + p3);
     w.m0 = mn0;
     w.m1 = mn1;
+    if (__any_sync(FULL_MASK, al0 != 1.f || al1 != 1.f)) {  // the running max moved
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        w.acc[i][0] *= al0;
-        w.acc[i][1] *= al1;
-        w.acc[i][2] *= al0;
-        w.acc[i][3] *= al1;
+        for (int i = 0; i < 8; ++i) {
+            w.acc[i][0] *= al0;
+            w.acc[i][1] *= al1;
+            w.acc[i][2] *= al0;
+            w.acc[i][3] *= al1;
+        }
     }
     const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // tokens 0-7
     const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // tokens 8-15
@@ -402,7 +494,8 @@ struct MergeSmem {
 // whole segment is inside this CTA, else this CTA's partial.
 __device__ __forceinline__ void flush_segment(const AttnOut& o, const MergeSmem& ms, WarpState& w,
                                               const Seg& sg, int s, long long c0, long long c1,
-                                              bool force_bad, int warp, int lane) {
+                                              size_t slot_base, bool force_bad, int warp,
+                                              int lane) {
     float l0 = w.l0, l1 = w.l1;
 #pragma unroll
     for (int off = 4; off <= 16; off <<= 1) {
@@ -461,7 +554,7 @@ __device__ __forceinline__ void flush_segment(const AttnOut& o, const MergeSmem&
             if (o.lse != nullptr && dd == 0)
                 o.lse[row] = (bad || empty) ? -INFINITY : (M + log2f(L)) * LN2;
         } else {
-            const size_t slot = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(s);
+            const size_t slot = slot_base + static_cast<size_t>(s);
             o.ws_o[(slot * G + h) * D + dd] = empty ? 0.f : O / L;
             if (dd == 0) o.ws_lse[slot * G + h] = bad ? INFINITY : (empty ? -INFINITY : M + log2f(L));
         }
@@ -483,58 +576,100 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
     int* gsm = reinterpret_cast<int*>(ms.o + ATTN_WARPS * o.G * OSTRIDE);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
     __syncthreads();
     const bool all_bad = geo.all_bad(gsm);
 
-    // The paged tile count is only known on the device: CTAs beyond it retire,
-    // so no CTA ever owns an empty range (the merge relies on that).
-    const long long N = geo.num_tiles(gsm);
-    const int C = static_cast<int>(min(static_cast<long long>(gridDim.x), N));
-    if (static_cast<int>(blockIdx.x) >= C) return;
-    const long long c0 = N * blockIdx.x / C, c1 = N * (blockIdx.x + 1) / C;
-    const int s_first = geo.seg_of(c0, gsm), s_last = geo.seg_of(c1 - 1, gsm);
+    // Every part is cut into C_p = min(C, tiles of the part) equal ranges;
+    // CTA c owns range c of every part (the paged tile count is only known on
+    // the device).  No CTA owns an empty range of a part it takes part in,
+    // which the partial merge relies on.
+    const int C = gridDim.x;
+    long long ra[Geo::kParts], rl[Geo::kParts];
+    long long total = 0;
+#pragma unroll
+    for (int p = 0; p < Geo::kParts; ++p) {
+        const long long np = geo.part_tiles(p, gsm);
+        const long long cp = min(static_cast<long long>(C), np);
+        ra[p] = geo.part_begin(p, gsm);
+        rl[p] = 0;
+        if (static_cast<long long>(blockIdx.x) < cp) {
+            ra[p] += np * blockIdx.x / cp;
+            rl[p] = geo.part_begin(p, gsm) + np * (blockIdx.x + 1) / cp - ra[p];
+        }
+        total += rl[p];
+    }
+    if (total == 0) return;  // uniform over the CTA
 
-    const long long my0 = c0 + warp;
-    const int nj = my0 < c1 ? static_cast<int>((c1 - my0 + ATTN_WARPS - 1) / ATTN_WARPS) : 0;
+    // Warp w takes the CTA's tiles w, w + 8, ... of the concatenated ranges.
+    auto tile_at = [&](long long u) -> long long {
+        return u < rl[0] ? ra[0] + u : ra[Geo::kParts - 1] + (u - rl[0]);
+    };
+    const int nj = warp < total ? static_cast<int>((total - warp + ATTN_WARPS - 1) / ATTN_WARPS) : 0;
     const uint32_t ring = smem_u32(smem) + warp * ATTN_STAGES * STAGE_BYTES;
     uint32_t* my_masks = masks + warp * ATTN_STAGES;
 
+    const uint64_t kv_policy = l2_evict_first_policy();
+    Cursor cur;
+    bool cur_part1 = false;
+    Pending pd;
+    auto prefetch = [&](int j) {
+        const long long u = warp + static_cast<long long>(j) * ATTN_WARPS;
+        const long long t = tile_at(u);
+        if (Geo::kParts > 1 && u >= rl[0] && !cur_part1) {
+            cursor_init(geo, gsm, t, cur);  // jump to this CTA's range of part 1
+            cur_part1 = true;
+        }
+        prefetch_tile(geo, gsm, t, lane, cur, pd);
+    };
+    cursor_init(geo, gsm, tile_at(min(static_cast<long long>(warp), total - 1)), cur);
+    cur_part1 = Geo::kParts > 1 && rl[0] == 0;
 #pragma unroll
     for (int j = 0; j < ATTN_STAGES - 1; ++j) {
-        if (j < nj)
-            issue_tile(geo, gsm, my0 + static_cast<long long>(j) * ATTN_WARPS,
-                       ring + j * STAGE_BYTES, my_masks + j, lane);
+        if (j < nj) {
+            prefetch(j);
+            issue_tile(geo, gsm, pd, ring + j * STAGE_BYTES, my_masks + j, lane, kv_policy);
+        }
         cp_async_commit();
     }
+    if (ATTN_STAGES - 1 < nj) prefetch(ATTN_STAGES - 1);
 
     int jc = 0;
     WarpState w;
-    for (int s = s_first; s <= s_last; ++s) {
-        const Seg sg = geo.segment(s, gsm);
-        if (sg.ntiles == 0) continue;  // empty requests are written before the launch loop
-        const long long seg_end = sg.first + sg.ntiles;
-        uint32_t qb[8][2];
-        load_q(o, sg, lane, qb);
-        state_reset(w);
-        while (jc < nj) {
-            const long long t = my0 + static_cast<long long>(jc) * ATTN_WARPS;
-            if (t >= seg_end) break;
-            cp_async_wait<ATTN_STAGES - 2>();
-            __syncwarp();
-            const int jn = jc + ATTN_STAGES - 1;
-            if (jn < nj)
-                issue_tile(geo, gsm, my0 + static_cast<long long>(jn) * ATTN_WARPS,
-                           ring + (jn % ATTN_STAGES) * STAGE_BYTES, my_masks + jn % ATTN_STAGES,
-                           lane);
-            cp_async_commit();
-            const int st = jc % ATTN_STAGES;
-            const uint32_t mw = *reinterpret_cast<volatile uint32_t*>(my_masks + st);
-            w.bad |= static_cast<int>(mw >> 16);
-            compute_tile(ring + st * STAGE_BYTES, mw & 0xffffu, qb, o.scale_log2, w, lane);
-            ++jc;
+#pragma unroll 1
+    for (int p = 0; p < Geo::kParts; ++p) {
+        if (rl[p] == 0) continue;
+        const long long c0 = ra[p], c1 = ra[p] + rl[p];
+        const int s_first = geo.seg_of(c0, gsm), s_last = geo.seg_of(c1 - 1, gsm);
+        for (int s = s_first; s <= s_last; ++s) {
+            const Seg sg = geo.segment(s, gsm);
+            if (sg.ntiles == 0) continue;  // empty requests are zeroed by a separate kernel
+            const long long seg_end = sg.first + sg.ntiles;
+            uint32_t qb[8][2];
+            load_q(o, sg, lane, qb);
+            state_reset(w);
+            while (jc < nj) {
+                const long long t = tile_at(warp + static_cast<long long>(jc) * ATTN_WARPS);
+                if (t >= seg_end) break;
+                cp_async_wait<ATTN_STAGES - 2>();
+                __syncwarp();
+                const int jn = jc + ATTN_STAGES - 1;
+                if (jn < nj)
+                    issue_tile(geo, gsm, pd, ring + (jn % ATTN_STAGES) * STAGE_BYTES,
+                               my_masks + jn % ATTN_STAGES, lane, kv_policy);
+                cp_async_commit();
+                if (jn + 1 < nj) prefetch(jn + 1);
+                const int st = jc % ATTN_STAGES;
+                const uint32_t mw = *reinterpret_cast<volatile uint32_t*>(my_masks + st);
+                w.bad |= static_cast<int>(mw >> 16);
+                compute_tile(ring + st * STAGE_BYTES, mw & 0xffffu, qb, o.scale_log2, w, lane);
+                ++jc;
+            }
+            flush_segment(o, ms, w, sg, s, c0, c1, blockIdx.x + static_cast<size_t>(p) * C,
+                          all_bad, warp, lane);
         }
-        flush_segment(o, ms, w, sg, s, c0, c1, all_bad, warp, lane);
     }
     cp_async_wait<0>();
 }
@@ -542,6 +677,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
 // Zeroes the outputs of requests with no tokens (paged only).
 __global__ void paged_zero_empty_kernel(const int32_t* __restrict__ ctx_len, int B, int max_tok,
                                         int Hq, clo_half* __restrict__ out, float* __restrict__ lse) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     if (r >= B) return;
     const int n = ctx_len[r];
@@ -556,66 +693,129 @@ __global__ void paged_zero_empty_kernel(const int32_t* __restrict__ ctx_len, int
 // Merges the per-CTA partials of every segment cut by a CTA boundary.  Block
 // i looks at the boundary between CTA i and i+1 and handles the segment that
 // straddles it if that segment starts inside CTA i (so each cut segment is
-// merged exactly once).
+// merged exactly once).  Thread (group, head, column) folds every ngrp-th
+// partial of 8 output columns in one online log-sum-exp pass, four partials
+// per trip with independent loads; the groups are then combined in shared
+// memory.
+constexpr int MERGE_COLS = 8;                  // floats per thread and partial
+constexpr int MERGE_ITEMS_PER_HEAD = D / MERGE_COLS;
+constexpr int MERGE_MAX_GROUPS = 32;
+constexpr int MERGE_UNROLL = 4;
+
+__device__ __forceinline__ int merge_groups(int G) {
+    const int g = MERGE_THREADS / (G * MERGE_ITEMS_PER_HEAD);
+    return g < MERGE_MAX_GROUPS ? g : MERGE_MAX_GROUPS;
+}
+
 template <class Geo>
-__global__ void __launch_bounds__(MERGE_THREADS)
+__global__ void __launch_bounds__(MERGE_THREADS, 1)
     attn_merge_kernel(const Geo geo, const AttnOut o, int C) {
     extern __shared__ __align__(16) uint8_t msmem[];
     const int G = o.G;
-    const int items = G * 32;             // (head, 4-float column)
-    const int ngrp = MERGE_THREADS / items;
-    float* Mg = reinterpret_cast<float*>(msmem);        // [ngrp][G]
-    float* Lg = Mg + ngrp * MAXG;                       // [ngrp][G]
-    int* Bg = reinterpret_cast<int*>(Lg + ngrp * MAXG); // [ngrp][G]
-    float4* Og = reinterpret_cast<float4*>(Bg + ngrp * MAXG);  // [ngrp][G][32]
-    int* gsm = reinterpret_cast<int*>(Og + ngrp * items);
+    const int items = G * MERGE_ITEMS_PER_HEAD;
+    const int ngrp = merge_groups(G);
+    float* Mg = reinterpret_cast<float*>(msmem);        // [ngrp][MAXG]
+    float* Lg = Mg + MERGE_MAX_GROUPS * MAXG;           // [ngrp][MAXG]
+    int* Bg = reinterpret_cast<int*>(Lg + MERGE_MAX_GROUPS * MAXG);
+    float4* Og = reinterpret_cast<float4*>(Bg + MERGE_MAX_GROUPS * MAXG);  // [ngrp][items][2]
+    int* gsm = reinterpret_cast<int*>(Og + 2 * MERGE_THREADS);
 
+    pdl_launch_dependents();
+    // Block (part, i) looks at the boundary between CTA ranges i and i + 1 of
+    // that part; partial slots of part `part` are offset by part * C.  With a
+    // static layout the test needs no shared state, so idle blocks leave at once
+    // (before waiting on the attention kernel: the test reads no memory).
+    if (Geo::kStaticLayout) {
+        const int part = blockIdx.x / (C - 1);
+        const int i = blockIdx.x - part * (C - 1);
+        const long long P0 = geo.part_begin(part, nullptr);
+        const long long N = geo.part_tiles(part, nullptr);
+        const long long Ce = min(static_cast<long long>(C), N);
+        if (i >= Ce - 1) return;
+        const long long start_i = P0 + N * i / Ce, tb = P0 + N * (i + 1) / Ce;
+        const long long first = geo.segment_first(geo.seg_of(tb, nullptr));
+        if (!(first < tb && first >= start_i)) return;
+    }
+    pdl_wait();
     geo.cta_init(gsm, nullptr, false);
     __syncthreads();
-    const long long N = geo.num_tiles(gsm);
-    const int Ce = static_cast<int>(min(static_cast<long long>(C), N));  // CTAs that had work
-    const int i = blockIdx.x;
+    const int part = blockIdx.x / (C - 1);
+    const int i = blockIdx.x - part * (C - 1);
+    const long long P0 = geo.part_begin(part, gsm);
+    const long long N = geo.part_tiles(part, gsm);
+    const int Ce = static_cast<int>(min(static_cast<long long>(C), N));  // CTAs with a range
     if (i >= Ce - 1) return;
-    const long long start_i = N * i / Ce, tb = N * (i + 1) / Ce;
+    const long long start_i = P0 + N * i / Ce, tb = P0 + N * (i + 1) / Ce;
     const int s = geo.seg_of(tb, gsm);
     const Seg sg = geo.segment(s, gsm);
     if (!(sg.first < tb && sg.first >= start_i)) return;
-    const long long last = sg.first + sg.ntiles - 1;
+    const long long last = sg.first + sg.ntiles - 1 - P0;
     const int c_hi = static_cast<int>(((last + 1) * Ce - 1) / N);
     const int P = c_hi - i + 1;
+    const size_t slot0 = static_cast<size_t>(i) + static_cast<size_t>(s) +
+                         static_cast<size_t>(part) * C;
 
     const int it = threadIdx.x % items, grp = threadIdx.x / items;
-    const int h = it >> 5, col = it & 31;
+    const int h = it / MERGE_ITEMS_PER_HEAD, col = it % MERGE_ITEMS_PER_HEAD;
     if (grp < ngrp) {
-        float M = -INFINITY;
+        float M = -INFINITY, L = 0.f;
+        float a[MERGE_COLS];
+#pragma unroll
+        for (int c = 0; c < MERGE_COLS; ++c) a[c] = 0.f;
         int bad = 0;
-        for (int p = grp; p < P; p += ngrp) {
-            const float x = o.ws_lse[(static_cast<size_t>(i + p) + s) * G + h];
-            if (x == INFINITY) bad = 1;
-            else M = fmaxf(M, x);
-        }
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-            for (int p = grp; p < P; p += ngrp) {
-                const size_t slot = static_cast<size_t>(i + p) + s;
-                const float x = o.ws_lse[slot * G + h];
-                if (x == INFINITY || x == -INFINITY) continue;
-                const float e = fast_exp2(x - M);
-                const float4 v = reinterpret_cast<const float4*>(o.ws_o + (slot * G + h) * D)[col];
-                L += e;
-                acc.x = fmaf(v.x, e, acc.x);
-                acc.y = fmaf(v.y, e, acc.y);
-                acc.z = fmaf(v.z, e, acc.z);
-                acc.w = fmaf(v.w, e, acc.w);
+        for (int p0 = grp; p0 < P; p0 += MERGE_UNROLL * ngrp) {
+            float x[MERGE_UNROLL];
+            float4 v0[MERGE_UNROLL], v1[MERGE_UNROLL];
+#pragma unroll
+            for (int u = 0; u < MERGE_UNROLL; ++u) {
+                const int p = p0 + u * ngrp;
+                x[u] = -INFINITY;
+                v0[u] = v1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p < P) {
+                    const size_t slot = slot0 + p;
+                    x[u] = o.ws_lse[slot * G + h];
+                    const float4* src =
+                        reinterpret_cast<const float4*>(o.ws_o + (slot * G + h) * D) + 2 * col;
+                    v0[u] = src[0];
+                    v1[u] = src[1];
+                }
             }
+            float mx = M;
+#pragma unroll
+            for (int u = 0; u < MERGE_UNROLL; ++u) {
+                if (x[u] == INFINITY) {
+                    bad = 1;
+                    x[u] = -INFINITY;
+                }
+                mx = fmaxf(mx, x[u]);
+            }
+            if (mx == -INFINITY) continue;
+            const float sc = fast_exp2(M - mx);
+            L *= sc;
+#pragma unroll
+            for (int c = 0; c < MERGE_COLS; ++c) a[c] *= sc;
+#pragma unroll
+            for (int u = 0; u < MERGE_UNROLL; ++u) {
+                const float e = fast_exp2(x[u] - mx);
+                L += e;
+                a[0] = fmaf(v0[u].x, e, a[0]);
+                a[1] = fmaf(v0[u].y, e, a[1]);
+                a[2] = fmaf(v0[u].z, e, a[2]);
+                a[3] = fmaf(v0[u].w, e, a[3]);
+                a[4] = fmaf(v1[u].x, e, a[4]);
+                a[5] = fmaf(v1[u].y, e, a[5]);
+                a[6] = fmaf(v1[u].z, e, a[6]);
+                a[7] = fmaf(v1[u].w, e, a[7]);
+            }
+            M = mx;
         }
         if (col == 0) {
             Mg[grp * MAXG + h] = M;
             Lg[grp * MAXG + h] = L;
             Bg[grp * MAXG + h] = bad;
         }
-        Og[grp * items + it] = acc;
+        Og[2 * (grp * items + it)] = make_float4(a[0], a[1], a[2], a[3]);
+        Og[2 * (grp * items + it) + 1] = make_float4(a[4], a[5], a[6], a[7]);
     }
     __syncthreads();
     if (grp == 0) {
@@ -626,29 +826,40 @@ __global__ void __launch_bounds__(MERGE_THREADS)
             bad |= Bg[g2 * MAXG + h];
         }
         float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float a[MERGE_COLS];
+#pragma unroll
+        for (int c = 0; c < MERGE_COLS; ++c) a[c] = 0.f;
         if (M != -INFINITY) {
             for (int g2 = 0; g2 < ngrp; ++g2) {
                 const float mg = Mg[g2 * MAXG + h];
                 if (mg == -INFINITY) continue;
                 const float e = fast_exp2(mg - M);
-                const float4 v = Og[g2 * items + it];
+                const float4 v0 = Og[2 * (g2 * items + it)];
+                const float4 v1 = Og[2 * (g2 * items + it) + 1];
                 L = fmaf(Lg[g2 * MAXG + h], e, L);
-                acc.x = fmaf(v.x, e, acc.x);
-                acc.y = fmaf(v.y, e, acc.y);
-                acc.z = fmaf(v.z, e, acc.z);
-                acc.w = fmaf(v.w, e, acc.w);
+                a[0] = fmaf(v0.x, e, a[0]);
+                a[1] = fmaf(v0.y, e, a[1]);
+                a[2] = fmaf(v0.z, e, a[2]);
+                a[3] = fmaf(v0.w, e, a[3]);
+                a[4] = fmaf(v1.x, e, a[4]);
+                a[5] = fmaf(v1.y, e, a[5]);
+                a[6] = fmaf(v1.z, e, a[6]);
+                a[7] = fmaf(v1.w, e, a[7]);
             }
         }
         const bool empty = !(L > 0.f);
         const size_t row = static_cast<size_t>(sg.b) * o.Hq + static_cast<size_t>(sg.kv) * G + h;
         const float inv = (bad || empty) ? 0.f : 1.f / L;
-        __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-        __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(o.out + row * D)[col] = pk;
+        uint4 pk;
+        __half2 h0 = __floats2half2_rn(a[0] * inv, a[1] * inv);
+        __half2 h1 = __floats2half2_rn(a[2] * inv, a[3] * inv);
+        __half2 h2 = __floats2half2_rn(a[4] * inv, a[5] * inv);
+        __half2 h3 = __floats2half2_rn(a[6] * inv, a[7] * inv);
+        pk.x = *reinterpret_cast<uint32_t*>(&h0);
+        pk.y = *reinterpret_cast<uint32_t*>(&h1);
+        pk.z = *reinterpret_cast<uint32_t*>(&h2);
+        pk.w = *reinterpret_cast<uint32_t*>(&h3);
+        reinterpret_cast<uint4*>(o.out + row * D)[col] = pk;
         if (o.lse != nullptr && col == 0)
             o.lse[row] = (bad || empty) ? -INFINITY : (M + log2f(L)) * LN2;
     }
@@ -670,26 +881,15 @@ static int device_sm_count() {
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Raises a kernel's dynamic shared-memory limit once per (kernel, device).
-static bool smem_attr_set(const void* func, int bytes) {
-    static std::mutex mu;
-    static const void* done_func[64];
-    static int done_dev[64];
-    static int n_done = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n_done; ++i)
-        if (done_func[i] == func && done_dev[i] == dev) return true;
-    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-        cudaSuccess)
-        return false;
-    if (n_done < 64) {
-        done_func[n_done] = func;
-        done_dev[n_done] = dev;
-        ++n_done;
-    }
-    return true;
+// Records a timing event on the stream.  Under stream capture the record is
+// made external so it becomes an event node of the graph (re-recorded on
+// every replay) rather than an internal ordering edge.
+static bool record_event(cudaEvent_t ev, cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return false;
+    if (cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal) == cudaSuccess;
+    return cudaEventRecord(ev, stream) == cudaSuccess;
 }
 
 static size_t partial_bytes(long long slots, int G) {
@@ -704,7 +904,7 @@ static size_t workspace_bytes(int B, int Hq, int Hkv, int d, int num_ctas) {
     if (G > MAXG) return 0;
     int C = num_ctas > 0 ? num_ctas : device_sm_count();
     if (C <= 0) return 0;
-    return partial_bytes(static_cast<long long>(C) + static_cast<long long>(B) * Hkv, G);
+    return partial_bytes(2ll * C + static_cast<long long>(B) * Hkv, G);
 }
 
 static size_t attn_smem_bytes(int G, size_t geo_ints) {
@@ -714,22 +914,22 @@ static size_t attn_smem_bytes(int G, size_t geo_ints) {
            geo_ints * sizeof(int);
 }
 
-static size_t merge_smem_bytes(int G, size_t geo_ints) {
-    const int items = G * 32;
-    const int ngrp = MERGE_THREADS / items;
-    return static_cast<size_t>(ngrp) * MAXG * 3 * sizeof(float) +
-           static_cast<size_t>(ngrp) * items * sizeof(float4) + geo_ints * sizeof(int);
+static size_t merge_smem_bytes(int /*G*/, size_t geo_ints) {
+    return static_cast<size_t>(MERGE_MAX_GROUPS) * MAXG * 3 * sizeof(float) +
+           static_cast<size_t>(2) * MERGE_THREADS * sizeof(float4) + geo_ints * sizeof(int);
 }
 
 template <class Geo>
 static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_host_bound,
                                    size_t geo_ints, int S, void* workspace, size_t ws_bytes,
                                    const clo_attn_opts* opts, cudaStream_t stream) {
-    if (!smem_attr_set(reinterpret_cast<const void*>(attn_split_kernel<Geo>), SMEM_LIMIT))
+    if (!prepare_kernel(reinterpret_cast<const void*>(attn_split_kernel<Geo>), SMEM_LIMIT) ||
+        !prepare_kernel(reinterpret_cast<const void*>(attn_merge_kernel<Geo>), MERGE_SMEM_LIMIT))
         return CLO_ERR_CUDA;
     const size_t smem = attn_smem_bytes(o.G, geo_ints);
     const size_t msmem = merge_smem_bytes(o.G, geo_ints);
-    if (smem > static_cast<size_t>(SMEM_LIMIT) || msmem > 48 * 1024) return CLO_ERR_UNSUPPORTED;
+    if (smem > static_cast<size_t>(SMEM_LIMIT) || msmem > static_cast<size_t>(MERGE_SMEM_LIMIT))
+        return CLO_ERR_UNSUPPORTED;
 
     int C = (opts != nullptr && opts->num_ctas > 0) ? opts->num_ctas : device_sm_count();
     if (C <= 0) return CLO_ERR_CUDA;
@@ -739,26 +939,24 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
     if (C > cap) C = static_cast<int>(cap > 0 ? cap : 1);
     if (C > n_tiles_host_bound) C = static_cast<int>(n_tiles_host_bound);
     if (C < 1) C = 1;
-    const size_t need = partial_bytes(static_cast<long long>(C) + S, o.G);
+    const long long slots = 2ll * C + S;  // room for one partial per (part, CTA, segment)
+    const size_t need = partial_bytes(slots, o.G);
     if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 16)) return CLO_ERR_WORKSPACE;
-    const long long slots = static_cast<long long>(C) + S;
     o.ws_o = static_cast<float*>(workspace);
     o.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                         ((static_cast<size_t>(slots) * o.G * D * sizeof(float) + 255) / 256) * 256);
 
-    // External records so that, under stream capture, they become event nodes
-    // of the graph (re-recorded on every replay).
-    if (opts != nullptr && opts->ev_begin != nullptr &&
-        cudaEventRecordWithFlags(opts->ev_begin, stream, cudaEventRecordExternal) != cudaSuccess)
+    if (opts != nullptr && opts->ev_begin != nullptr && !record_event(opts->ev_begin, stream))
         return CLO_ERR_CUDA;
-    attn_split_kernel<Geo><<<C, ATTN_THREADS, smem, stream>>>(geo, o);
-    if (cudaGetLastError() != cudaSuccess) return CLO_ERR_CUDA;
-    if (opts != nullptr && opts->ev_end != nullptr &&
-        cudaEventRecordWithFlags(opts->ev_end, stream, cudaEventRecordExternal) != cudaSuccess)
+    if (launch_pdl(attn_split_kernel<Geo>, dim3(C), dim3(ATTN_THREADS), smem, stream, geo, o) !=
+        cudaSuccess)
+        return CLO_ERR_CUDA;
+    if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
     if (C >= 2) {
-        attn_merge_kernel<Geo><<<C - 1, MERGE_THREADS, msmem, stream>>>(geo, o, C);
-        if (cudaGetLastError() != cudaSuccess) return CLO_ERR_CUDA;
+        if (launch_pdl(attn_merge_kernel<Geo>, dim3(Geo::kParts * (C - 1)), dim3(MERGE_THREADS),
+                       msmem, stream, geo, o, C) != cudaSuccess)
+            return CLO_ERR_CUDA;
     }
     return CLO_OK;
 }
@@ -791,6 +989,7 @@ extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* 
     const int G = Hq / Hkv;
     if (d != D || G > MAXG || Hkv > MAX_HKV_HYBRID) return CLO_ERR_UNSUPPORTED;
     const bool has_cb = Np < Hkv;
+    if (C > MAX_ROWS || T > MAX_ROWS) return CLO_ERR_UNSUPPORTED;
     if (has_cb) {
         if (cbK == nullptr || cbV == nullptr || idx == nullptr || k < 1 || C < k)
             return CLO_ERR_INVALID_ARG;
@@ -819,9 +1018,9 @@ extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* 
     geo.Hkv = Hkv;
     geo.tp = Np > 0 ? (T + TILE - 1) / TILE : 1;
     geo.tc = has_cb ? (k + TILE - 1) / TILE : 1;
-    geo.per_b = static_cast<long long>(Np) * (Np > 0 ? geo.tp : 0) +
-                static_cast<long long>(Hkv - Np) * (has_cb ? geo.tc : 0);
-    const long long N = geo.per_b * B;
+    geo.n0 = static_cast<long long>(B) * Np * (Np > 0 ? geo.tp : 0);
+    geo.n1 = static_cast<long long>(B) * (Hkv - Np) * (has_cb ? geo.tc : 0);
+    const long long N = geo.n0 + geo.n1;
 
     AttnOut o{};
     o.q = q;
@@ -875,8 +1074,11 @@ extern "C" clo_status clo_paged_decode_attn(const clo_half* q, const clo_half* k
     o.Hq = Hq;
     o.G = G;
     // Requests with no tokens (or an invalid length) get zeros before the main kernel.
-    paged_zero_empty_kernel<<<B, 128, 0, stream>>>(ctx_len, B, max_blocks * TILE, Hq, out, lse);
-    if (cudaGetLastError() != cudaSuccess) return CLO_ERR_CUDA;
+    if (!prepare_kernel(reinterpret_cast<const void*>(paged_zero_empty_kernel), 0))
+        return CLO_ERR_CUDA;
+    if (launch_pdl(paged_zero_empty_kernel, dim3(B), dim3(128), 0, stream, ctx_len, B,
+                   max_blocks * TILE, Hq, out, lse) != cudaSuccess)
+        return CLO_ERR_CUDA;
     // The tile count depends on device-resident lengths; size the grid for the
     // largest possible stream (CTAs never exceed the true count, see kernel).
     const long long bound = static_cast<long long>(B) * Hkv * max_blocks;

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+
 #include "clo.h"
 
 namespace clo {
@@ -22,6 +25,23 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                  "r"(src_bytes)
+                 : "memory");
+}
+
+// L2 policy for data read exactly once (the K/V stream): evict it first, so
+// streaming hundreds of MB through L2 does not push out kernel code,
+// parameters and the small tensors the surrounding kernels reuse.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+
+// cp_async_16 with an L2 cache-policy hint.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, int src_bytes,
+                                                 uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+                 "l"(src), "r"(src_bytes), "l"(policy)
                  : "memory");
 }
 
@@ -73,6 +93,64 @@ __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
 __device__ __forceinline__ void report_error(int32_t* err_flag, int bits) {
     if (err_flag != nullptr) atomicOr(reinterpret_cast<int*>(err_flag), bits);
+}
+
+// Programmatic dependent launch.  Every libclo kernel is launched with
+// programmatic stream serialisation, lets its dependents start launching at
+// once (launch_dependents) and waits for its predecessor grid to complete and
+// flush (griddepcontrol.wait) before its first global-memory access.  The
+// next kernel's launch and scheduling thus overlap the current one's tail,
+// while ordering stays transitive: no kernel touches memory before every
+// kernel ahead of it in the stream has finished.  For a predecessor launched
+// without the attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" :::);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Applies the launch attributes every libclo kernel shares, once per
+// (kernel, device): the maximum shared-memory carveout (so consecutive libclo
+// kernels never make the SMs switch their L1/shared split) and, if
+// dyn_smem > 48 KB, the opt-in dynamic shared-memory size.
+inline bool prepare_kernel(const void* func, int dyn_smem) {
+    static std::mutex mu;
+    static const void* done_func[64];
+    static int done_dev[64];
+    static int n_done = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done_func[i] == func && done_dev[i] == dev) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return false;
+    if (dyn_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem) !=
+            cudaSuccess)
+        return false;
+    if (n_done < 64) {
+        done_func[n_done] = func;
+        done_dev[n_done] = dev;
+        ++n_done;
+    }
+    return true;
 }
 
 }  // namespace clo

@@ -29,6 +29,8 @@ constexpr float PI_F = 3.14159265358979323846f;
 
 __global__ void thresholds_kernel(const float* __restrict__ s, int n_kv, int group, float eta,
                                   float n_exp, float* __restrict__ tau) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= n_kv) return;
     float acc = 0.f;
@@ -62,6 +64,8 @@ __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS)
     lookup_update_kernel(const LookupParams p) {
     extern __shared__ uint8_t miss_sm[];  // miss bit of each group of this CTA
     __shared__ int cta_misses;
+    pdl_launch_dependents();
+    pdl_wait();
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
     const int ngroups = p.B * p.Hkv;
@@ -75,14 +79,19 @@ __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS)
         const int g = gi - b * p.Hkv;
         const size_t base = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G) * 128 +
                             static_cast<size_t>(lane) * 4;
+        // Every load of the group is issued before the first use.
         uint2 qv[LK_MAX_G], lv[LK_MAX_G];
+        float wv[LK_MAX_G];
 #pragma unroll
         for (int j = 0; j < LK_MAX_G; ++j) {
             if (j < p.G) {
                 qv[j] = *reinterpret_cast<const uint2*>(p.q + base + j * 128);
                 lv[j] = *reinterpret_cast<const uint2*>(p.labels + base + j * 128);
+                wv[j] = __ldg(p.w + g * p.G + j);
             }
         }
+        const float tau_g = __ldg(p.tau + g);
+        const bool persistent = p.pmask != nullptr && __ldg(p.pmask + g) != 0;
         float sw = 0.f, swc = 0.f, sc = 0.f;
 #pragma unroll
         for (int j = 0; j < LK_MAX_G; ++j) {
@@ -108,7 +117,7 @@ __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS)
                     ll += __shfl_xor_sync(FULL_MASK, ll, off);
                 }
                 const float c = (qq > 0.f && ll > 0.f) ? dot / (sqrtf(qq) * sqrtf(ll)) : 0.f;
-                const float w = p.w[g * p.G + j];
+                const float w = wv[j];
                 sw += w;
                 swc = fmaf(w, c, swc);
                 sc += c;
@@ -116,9 +125,9 @@ __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS)
         }
         const float s = (sw != 0.f) ? swc / sw : sc / static_cast<float>(p.G);  // Eq. 10
         uint8_t f;
-        if (p.pmask != nullptr && p.pmask[g] != 0) {
+        if (persistent) {
             f = 2;  // persistent: always resident, never looked up
-        } else if (s >= p.tau[g]) {
+        } else if (s >= tau_g) {
             f = 0;  // hit: keep the label
         } else {
             f = 1;  // miss: the whole KV head is replaced, labels <- current queries
@@ -171,8 +180,11 @@ extern "C" clo_status clo_thresholds(const float* s, int n_kv, int group, float 
     if (n_kv == 0) return CLO_OK;
     const int threads = 128;
     const int blocks = (n_kv + threads - 1) / threads;
-    thresholds_kernel<<<blocks, threads, 0, stream>>>(s, n_kv, group, eta, n_exp, tau);
-    return cudaGetLastError() == cudaSuccess ? CLO_OK : CLO_ERR_CUDA;
+    if (!prepare_kernel(reinterpret_cast<const void*>(thresholds_kernel), 0)) return CLO_ERR_CUDA;
+    return launch_pdl(thresholds_kernel, dim3(blocks), dim3(threads), 0, stream, s, n_kv, group,
+                      eta, n_exp, tau) == cudaSuccess
+               ? CLO_OK
+               : CLO_ERR_CUDA;
 }
 
 extern "C" clo_status clo_lookup_update(const clo_half* q, clo_half* labels, const float* w_q,
@@ -199,6 +211,10 @@ extern "C" clo_status clo_lookup_update(const clo_half* q, clo_half* labels, con
     LookupParams p{q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count,
                    B, Hq, Hkv, G};
     const int per_cta = (B * Hkv + LK_CLUSTER - 1) / LK_CLUSTER;
-    lookup_update_kernel<<<LK_CLUSTER, LK_THREADS, static_cast<size_t>(per_cta), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CLO_OK : CLO_ERR_CUDA;
+    if (!prepare_kernel(reinterpret_cast<const void*>(lookup_update_kernel), per_cta))
+        return CLO_ERR_CUDA;
+    return launch_pdl(lookup_update_kernel, dim3(LK_CLUSTER), dim3(LK_THREADS),
+                      static_cast<size_t>(per_cta), stream, p) == cudaSuccess
+               ? CLO_OK
+               : CLO_ERR_CUDA;
 }

@@ -42,9 +42,10 @@ def test_status_helpers(L):
 
 
 def test_workspace_size_formula(L):
-    # (CTAs + B*Hkv) partial slots of G*(128 floats + 1 lse), each array padded to 256 B.
+    # (2 * CTAs + B*Hkv) partial slots (one per part, CTA and token set) of
+    # G*(128 floats + 1 lse), each array padded to 256 B.
     def expect(B, Hq, Hkv, C):
-        slots = C + B * Hkv
+        slots = 2 * C + B * Hkv
         G = Hq // Hkv
         o = slots * G * 128 * 4
         l = slots * G * 4
