@@ -169,6 +169,39 @@ clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
                                   const clo_attn_opts* opts,
                                   cudaStream_t stream);
 
+/*
+ * clo_hybrid_decode_attn_noalloc -- clo_hybrid_decode_attn for callers that
+ * cannot allocate device memory: code running while its stream is captured
+ * into a CUDA graph (an allocation would break the capture), engines that own
+ * all device memory through their own pool, or deployments that forbid
+ * allocation after start-up.  The pages have no counterpart: this is a
+ * deployment variant of the same computation.
+ * Same arguments, layouts and results as clo_hybrid_decode_attn, without the
+ * workspace: the split-KV scratch is a fixed array of
+ * clo_hybrid_noalloc_max_scratch() bytes (8 MiB) compiled into the library,
+ * which every GPU that loads the library holds until the process exits.
+ *  - Returns CLO_ERR_WORKSPACE, launching nothing, when the problem needs more
+ *    than that (clo_hybrid_workspace_size(B, Hq, Hkv, d, num_ctas) > 8 MiB).
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.  CLO_ERR_CUDA if the lookup fails.
+ *  - It never calls cudaMalloc, cudaFree or any allocating routine.
+ *  - All calls share the one array and it keeps the previous call's
+ *    contents; nothing in it needs to start at zero.  Calls that overlap on
+ *    the GPU (concurrent streams, or devices sharing a context) race on it:
+ *    serialise them.
+ */
+clo_status clo_hybrid_decode_attn_noalloc(const clo_half* q, const clo_half* cbK,
+                                          const clo_half* cbV, const int32_t* idx, int k, int C,
+                                          const clo_half* pK, const clo_half* pV,
+                                          const int32_t* persist_ids, int Np, int T, int B,
+                                          int Hq, int Hkv, int d, float scale, clo_half* out,
+                                          float* lse, int32_t* err_flag,
+                                          const clo_attn_opts* opts, cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch used by clo_hybrid_decode_attn_noalloc. */
+size_t clo_hybrid_noalloc_max_scratch(void);
+
 /* Workspace bytes clo_paged_decode_attn needs (same rules as above). */
 size_t clo_paged_workspace_size(int B, int Hq, int Hkv, int d, int num_ctas);
 

@@ -57,6 +57,9 @@ _SIGS = {
     "clo_hybrid_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_hybrid_decode_attn": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _F, _P, _P, _P, _SZ, _P, _P, _P], _I),
+    "clo_hybrid_decode_attn_noalloc": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I,
+                                        _I, _F, _P, _P, _P, _P, _P], _I),
+    "clo_hybrid_noalloc_max_scratch": ([], _SZ),
     "clo_paged_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_paged_decode_attn": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                _P, _SZ, _P, _P, _P], _I),
@@ -267,3 +270,51 @@ def clo_paged_decode_attn(q: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor,
         float(scale), pout, plse, pws, workspace.numel(), perr,
         ctypes.byref(opts) if opts is not None else None, _stream(stream)),
         "clo_paged_decode_attn")
+
+
+def clo_hybrid_noalloc_max_scratch() -> int:
+    """Bytes of the fixed scratch behind clo_hybrid_decode_attn_noalloc."""
+    return int(lib().clo_hybrid_noalloc_max_scratch())
+
+
+def clo_hybrid_decode_attn_noalloc(q: torch.Tensor, cbK: Optional[torch.Tensor],
+                                   cbV: Optional[torch.Tensor], idx: Optional[torch.Tensor],
+                                   pK: Optional[torch.Tensor], pV: Optional[torch.Tensor],
+                                   persist_ids: Optional[torch.Tensor], out: torch.Tensor,
+                                   lse: Optional[torch.Tensor] = None,
+                                   err_flag: Optional[torch.Tensor] = None,
+                                   scale: Optional[float] = None, num_ctas: int = 0,
+                                   events: Optional[Sequence] = None, stream=None):
+    """clo_hybrid_decode_attn without a caller workspace, for callers that
+    cannot allocate device memory at call time (e.g. under CUDA-graph capture
+    or with an engine-owned memory pool): the library's fixed 8 MiB scratch is
+    used instead.  Raises CloError(CLO_ERR_WORKSPACE) for problems needing
+    more; calls that overlap on the GPU share that scratch and must be
+    serialised."""
+    pq = _dev(q, "q", torch.float16, 3)
+    B, Hq, d = q.shape
+    Np = 0 if persist_ids is None else persist_ids.numel()
+    if cbK is not None:
+        Hkv, C = cbK.shape[1], cbK.shape[2]
+        k = idx.shape[2] if idx is not None else 0
+    else:
+        Hkv, C, k = Np, 0, 0
+    T = pK.shape[2] if (pK is not None and Np > 0) else 0
+    pcbk = _dev(cbK, "cbK", torch.float16, 4, optional=True)
+    pcbv = _dev(cbV, "cbV", torch.float16, 4, optional=True)
+    pidx = _dev(idx, "idx", torch.int32, 3, optional=True)
+    ppk = _dev(pK, "pK", torch.float16, 4, optional=True) if Np > 0 else 0
+    ppv = _dev(pV, "pV", torch.float16, 4, optional=True) if Np > 0 else 0
+    ppid = _dev(persist_ids, "persist_ids", torch.int32, optional=True) if Np > 0 else 0
+    pout = _dev(out, "out", torch.float16, 3)
+    plse = _dev(lse, "lse", torch.float32, optional=True)
+    perr = _dev(err_flag, "err_flag", torch.int32, optional=True)
+    if out.shape != q.shape or (lse is not None and lse.numel() != B * Hq):
+        raise CloError("out / lse shapes do not match q", CLO_ERR_INVALID_ARG)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_hybrid_decode_attn_noalloc(
+        pq, pcbk, pcbv, pidx, k, C, ppk, ppv, ppid, Np, T, B, Hq, Hkv, d, float(scale),
+        pout, plse, perr, ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "clo_hybrid_decode_attn_noalloc")

@@ -37,6 +37,8 @@
 //    is ORed into err_flag and the affected outputs are written as zeros.
 #include <math.h>
 
+#include <mutex>
+
 #include "clo_device.cuh"
 
 namespace clo {
@@ -1084,4 +1086,54 @@ extern "C" clo_status clo_paged_decode_attn(const clo_half* q, const clo_half* k
     const long long bound = static_cast<long long>(B) * Hkv * max_blocks;
     return launch_attention(geo, o, bound, PagedGeo::smem_ints(Hkv, B), B * Hkv, workspace,
                             ws_bytes, opts, stream);
+}
+
+// ---------------------------------------------------------------- no-allocation variant
+// Some callers cannot allocate device memory when they run this path: code
+// that executes while its stream is being captured into a CUDA graph (an
+// allocation there fails the capture), engines that hand every byte of the
+// GPU to their own pool and forbid outside allocations, and deployments that
+// freeze allocation after start-up.  clo_hybrid_decode_attn_noalloc serves
+// them: its split-KV scratch is the fixed array below, part of the library
+// image, which every GPU that loads the library keeps until the process exits.
+namespace clo {
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device with that device current, then cached.
+static void* noalloc_scratch_address() {
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+}  // namespace clo
+
+extern "C" size_t clo_hybrid_noalloc_max_scratch(void) { return clo::NOALLOC_SCRATCH_BYTES; }
+
+extern "C" clo_status clo_hybrid_decode_attn_noalloc(
+    const clo_half* q, const clo_half* cbK, const clo_half* cbV, const int32_t* idx, int k, int C,
+    const clo_half* pK, const clo_half* pV, const int32_t* persist_ids, int Np, int T, int B,
+    int Hq, int Hkv, int d, float scale, clo_half* out, float* lse, int32_t* err_flag,
+    const clo_attn_opts* opts, cudaStream_t stream) {
+    if (B == 0)
+        return clo_hybrid_decode_attn(q, cbK, cbV, idx, k, C, pK, pV, persist_ids, Np, T, B, Hq,
+                                      Hkv, d, scale, out, lse, nullptr, 0, err_flag, opts, stream);
+    const int num_ctas = opts != nullptr ? opts->num_ctas : 0;
+    const size_t need = clo_hybrid_workspace_size(B, Hq, Hkv, d, num_ctas);
+    if (need > clo::NOALLOC_SCRATCH_BYTES) return CLO_ERR_WORKSPACE;  // problem too large
+    void* scratch = clo::noalloc_scratch_address();
+    if (scratch == nullptr) return CLO_ERR_CUDA;
+    return clo_hybrid_decode_attn(q, cbK, cbV, idx, k, C, pK, pV, persist_ids, Np, T, B, Hq, Hkv,
+                                  d, scale, out, lse, scratch, clo::NOALLOC_SCRATCH_BYTES,
+                                  err_flag, opts, stream);
 }
