@@ -30,6 +30,7 @@ a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -210,8 +211,7 @@ class PagedWorkload:
         import offloaded_kv_decode_gb300 as clo
 
         self.clo, self.torch = clo, torch
-        self.cfg = pc if rank == 0 else wl.PagedConfig(pc.name, pc.B, pc.Hq, pc.Hkv, pc.ctx_lo,
-                                                       pc.ctx_hi, seed=pc.seed + 1000 * rank)
+        self.cfg = pc if rank == 0 else dataclasses.replace(pc, seed=pc.seed + 1000 * rank)
         self.L = 1
         self.q, self.kc, self.vc, self.bt, self.ctx = wl.paged_inputs(self.cfg, dev)
         self.ctx_np = self.ctx.cpu().numpy()
@@ -465,9 +465,15 @@ def run_ours(args):
 
     clo.lib()
     if args.workload in wl.CONFIGS:
-        W = HybridWorkload(wl.CONFIGS[args.workload], dev, rank, args.replicas)
+        cfg = wl.CONFIGS[args.workload]
+        if args.batch:
+            cfg = dataclasses.replace(cfg, B=args.batch)
+        W = HybridWorkload(cfg, dev, rank, args.replicas)
     else:
-        W = PagedWorkload(wl.PAGED_CONFIGS[args.workload], dev, rank)
+        pc = wl.PAGED_CONFIGS[args.workload]
+        if args.batch:
+            pc = dataclasses.replace(pc, B=args.batch)
+        W = PagedWorkload(pc, dev, rank)
     stream = torch.cuda.current_stream(dev)
 
     # Eager warm-up (sets kernel attributes before capture).
@@ -671,6 +677,8 @@ def main(argv=None):
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--replicas", type=int, default=0,
                     help="physical buffer sets of a one-layer workload (0 = auto, >1 GB apart)")
     args = ap.parse_args(argv)
