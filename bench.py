@@ -85,12 +85,14 @@ def paged_bytes(pc, ctx: np.ndarray) -> int:
 class HybridWorkload:
     kind = "hybrid"
 
-    def __init__(self, cfg, dev, rank: int, replicas: int = 0):
+    def __init__(self, cfg, dev, rank: int, replicas: int = 0, overlap: bool = True):
         import torch
         import offloaded_kv_decode_gb300 as clo
 
         self.clo, self.torch = clo, torch
         self.cfg = cfg
+        self.overlap = overlap
+        self.side = torch.cuda.Stream(dev)
         self.L = cfg.L
         per_layer = hybrid_attn_bytes(cfg)
         if cfg.L > 1:
@@ -143,19 +145,56 @@ class HybridWorkload:
     def launches_per_step(self) -> int:
         return 1 + self.L * (1 + self.attn_kernels)
 
+    def _lookup(self, step: int, l: int):
+        cfg = self.cfg
+        it = self.instance(step, l)
+        j = (step * self.L + l) % self.n_inst
+        tau = self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv]
+        self.clo.clo_lookup_update(it["q"], it["labels"], it["w"], tau, it["pmask"], it["flag"],
+                                   it["sim"], it["miss"], it["nmiss"])
+
+    def _attention(self, step: int, l: int, events=None):
+        it = self.instance(step, l)
+        self.clo.clo_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"],
+                                        it["pV"], it["pid"], it["out"], self.ws,
+                                        err_flag=self.err, events=events)
+
     def launch(self, step: int, attn_events=None):
-        clo, cfg = self.clo, self.cfg
-        clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+        """One decode step.  With overlap (the default) the lookup runs one
+        layer ahead on a second stream, as in CLO's decode flow: the lookup of
+        layer l+1 starts when layer l starts (after attention l-1) and runs
+        beside attention l, and the step's last lookup is the next step's
+        layer 0 (replays of the step graph are ordered on the stream, so
+        attention 0 of a step always follows its lookup).  Each step still
+        runs exactly L lookups and L attentions.  Without overlap every layer
+        runs lookup then attention on one stream."""
+        clo, cfg, torch = self.clo, self.cfg, self.torch
+        if not self.overlap:
+            clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+            for l in range(self.L):
+                self._lookup(step, l)
+                self._attention(step, l, None if attn_events is None else attn_events[l])
+            return
+        main = torch.cuda.current_stream()
+        side = self.side
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        looked = [torch.cuda.Event() for _ in range(self.L + 1)]
+        attn_done = [torch.cuda.Event() for _ in range(self.L)]
+        with torch.cuda.stream(side):
+            clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
         for l in range(self.L):
-            it = self.instance(step, l)
-            j = (step * self.L + l) % self.n_inst
-            tau = self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv]
-            clo.clo_lookup_update(it["q"], it["labels"], it["w"], tau, it["pmask"], it["flag"],
-                                  it["sim"], it["miss"], it["nmiss"])
-            clo.clo_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"],
-                                       it["pV"], it["pid"], it["out"], self.ws,
-                                       err_flag=self.err,
-                                       events=None if attn_events is None else attn_events[l])
+            with torch.cuda.stream(side):
+                if l >= 1:
+                    side.wait_event(attn_done[l - 1])
+                self._lookup(step, l + 1)  # layer l+1; for l = L-1 the next step's layer 0
+                looked[l + 1].record(side)
+            if l >= 1:
+                main.wait_event(looked[l])
+            self._attention(step, l, None if attn_events is None else attn_events[l])
+            attn_done[l].record(main)
+        main.wait_stream(side)
 
     # e2e: per layer, H2D of the new queries, the two calls, D2H of the
     # attention output and the lookup results (flags, sims, miss list).
@@ -194,6 +233,8 @@ class HybridWorkload:
         return {"workload": c.name, "batch": c.B, "layers": c.L, "q_heads": c.Hq,
                 "kv_heads": c.Hkv, "head_dim": c.d, "context": c.T, "top_k": c.k,
                 "persistent_heads": c.Np, "cache_buffer": c.addressing,
+                "lookup_schedule": ("one layer ahead on a second stream" if self.overlap
+                                    else "before each layer's attention, same stream"),
                 "physical_buffer_sets": self.n_inst,
                 "l2": f"inputs larger than L2: a buffer is re-read after "
                       f"{self.reuse_distance() / 2**30:.2f} GiB of other reads"}
@@ -468,7 +509,7 @@ def run_ours(args):
         cfg = wl.CONFIGS[args.workload]
         if args.batch:
             cfg = dataclasses.replace(cfg, B=args.batch)
-        W = HybridWorkload(cfg, dev, rank, args.replicas)
+        W = HybridWorkload(cfg, dev, rank, args.replicas, overlap=not args.no_lookup_overlap)
     else:
         pc = wl.PAGED_CONFIGS[args.workload]
         if args.batch:
@@ -677,6 +718,8 @@ def main(argv=None):
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-lookup-overlap", action="store_true",
+                    help="run lookup and attention of each layer back to back on one stream")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--replicas", type=int, default=0,

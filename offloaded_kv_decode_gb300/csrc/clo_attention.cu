@@ -37,6 +37,7 @@
 //    is ORed into err_flag and the affected outputs are written as zeros.
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "clo_device.cuh"
@@ -50,14 +51,15 @@ constexpr int KV_TILE_BYTES = TILE * ROW_BYTES;  // 4 KB of K (or V) per tile
 constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;   // K + V
 constexpr int MAXG = 8;
 constexpr int OSTRIDE = D + 4;  // padded merge-area row (floats): conflict-free writes
-constexpr int ATTN_WARPS = 8;
+constexpr int ATTN_WARPS = 4;
+constexpr int ATTN_CTAS_PER_SM = 2;
 constexpr int ATTN_STAGES = 3;
 constexpr int ATTN_THREADS = ATTN_WARPS * 32;
 constexpr int MERGE_THREADS = 512;
 constexpr int MAX_HKV_HYBRID = 64;
 constexpr int MAX_PAGED_B = 4096;
 constexpr int MAX_ROWS = 1 << 24;  // rows per head: row offsets stay 32-bit
-constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int SMEM_LIMIT = 113 * 1024;  // two CTAs per SM
 constexpr int MERGE_SMEM_LIMIT = 96 * 1024;
 
 // One token set: batch row (or request) b, KV head kv.
@@ -157,6 +159,16 @@ struct HybridGeo {
         return s < B * Np ? static_cast<long long>(s) * tp
                           : n0 + static_cast<long long>(s - B * Np) * tc;
     }
+    __device__ int segment_part(int s) const { return s < B * Np ? 0 : 1; }
+    // Upper bound on the CTA ranges one token set can span (host side).
+    long long max_partials_host(int C) const {
+        long long most = 1;
+        if (n0 > 0) most = std::max(most, (static_cast<long long>(tp) * C + n0 - 1) / n0 + 1);
+        if (n1 > 0) most = std::max(most, (static_cast<long long>(tc) * C + n1 - 1) / n1 + 1);
+        return most;
+    }
+    __device__ int segment_ntiles(int s) const { return s < B * Np ? tp : tc; }
+    __host__ __device__ int num_segments() const { return B * Hkv; }
     __device__ Seg segment(int s, const int* sm) const {
         Seg g;
         int slot;
@@ -297,6 +309,11 @@ struct PagedGeo {
         return r * Hkv + static_cast<int>((t - sm[r]) / tr);
     }
     __device__ long long segment_first(int) const { return 0; }  // unused: layout is dynamic
+    __device__ int segment_part(int) const { return 0; }
+    // Lengths live on the device: assume the worst case (one head per block).
+    long long max_partials_host(int C) const { return static_cast<long long>(C); }
+    __device__ int segment_ntiles(int) const { return 0; }
+    __host__ __device__ int num_segments() const { return B * Hkv; }
     __device__ Seg segment(int s, const int* sm) const {
         Seg g;
         g.b = s / Hkv;
@@ -565,7 +582,7 @@ __device__ __forceinline__ void flush_segment(const AttnOut& o, const MergeSmem&
 }
 
 template <class Geo>
-__global__ void __launch_bounds__(ATTN_THREADS, 1)
+__global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     attn_split_kernel(const Geo geo, const AttnOut o) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int RING = ATTN_WARPS * ATTN_STAGES * STAGE_BYTES;
@@ -692,73 +709,79 @@ __global__ void paged_zero_empty_kernel(const int32_t* __restrict__ ctx_len, int
             lse[static_cast<size_t>(r) * Hq + h] = -INFINITY;
 }
 
-// Merges the per-CTA partials of every segment cut by a CTA boundary.  Block
-// i looks at the boundary between CTA i and i+1 and handles the segment that
-// straddles it if that segment starts inside CTA i (so each cut segment is
-// merged exactly once).  Thread (group, head, column) folds every ngrp-th
-// partial of 8 output columns in one online log-sum-exp pass, four partials
-// per trip with independent loads; the groups are then combined in shared
-// memory.
-constexpr int MERGE_COLS = 8;                  // floats per thread and partial
-constexpr int MERGE_ITEMS_PER_HEAD = D / MERGE_COLS;
-constexpr int MERGE_MAX_GROUPS = 32;
-constexpr int MERGE_UNROLL = 4;
-
-__device__ __forceinline__ int merge_groups(int G) {
-    const int g = MERGE_THREADS / (G * MERGE_ITEMS_PER_HEAD);
-    return g < MERGE_MAX_GROUPS ? g : MERGE_MAX_GROUPS;
-}
+// Merges the per-CTA partials of every token set cut by CTA boundaries.  A
+// block handles `hpb` query heads of one cut token set (the host picks all G
+// heads when every set has few partials, one head per block when some set
+// has many).  Thread (group, head, column) folds every ngrp-th partial of 8
+// output columns in one online log-sum-exp pass, eight partials per trip with
+// independent loads; the groups are then combined in shared memory.
+constexpr int MERGE_COLS = 8;                                   // floats per thread and partial
+constexpr int MERGE_ITEMS = D / MERGE_COLS;                     // 16 column groups per head
+constexpr int MERGE_MAX_GROUPS = MERGE_THREADS / MERGE_ITEMS;   // 32 partial subsets
+constexpr int MERGE_UNROLL = 8;                                 // independent partials per trip
 
 template <class Geo>
 __global__ void __launch_bounds__(MERGE_THREADS, 1)
-    attn_merge_kernel(const Geo geo, const AttnOut o, int C) {
+    attn_merge_kernel(const Geo geo, const AttnOut o, int C, int hpb) {
     extern __shared__ __align__(16) uint8_t msmem[];
+    // Block (x, y) merges query heads [y * hpb, (y + 1) * hpb) of one cut token set.
     const int G = o.G;
-    const int items = G * MERGE_ITEMS_PER_HEAD;
-    const int ngrp = merge_groups(G);
-    float* Mg = reinterpret_cast<float*>(msmem);        // [ngrp][MAXG]
-    float* Lg = Mg + MERGE_MAX_GROUPS * MAXG;           // [ngrp][MAXG]
-    int* Bg = reinterpret_cast<int*>(Lg + MERGE_MAX_GROUPS * MAXG);
+    const int items = hpb * MERGE_ITEMS;
+    const int ngrp = min(MERGE_THREADS / items, MERGE_MAX_GROUPS);
+    float* Mg = reinterpret_cast<float*>(msmem);                     // [ngrp][MAXG]
+    float* Lg = Mg + MERGE_MAX_GROUPS * MAXG;                        // [ngrp][MAXG]
+    int* Bg = reinterpret_cast<int*>(Lg + MERGE_MAX_GROUPS * MAXG);  // [ngrp][MAXG]
     float4* Og = reinterpret_cast<float4*>(Bg + MERGE_MAX_GROUPS * MAXG);  // [ngrp][items][2]
     int* gsm = reinterpret_cast<int*>(Og + 2 * MERGE_THREADS);
 
     pdl_launch_dependents();
-    // Block (part, i) looks at the boundary between CTA ranges i and i + 1 of
-    // that part; partial slots of part `part` are offset by part * C.  With a
-    // static layout the test needs no shared state, so idle blocks leave at once
-    // (before waiting on the attention kernel: the test reads no memory).
+    // Static layouts (hybrid): block s handles token set s if CTA boundaries
+    // cut it; the test needs no memory, so blocks with nothing to merge leave
+    // at once.  Dynamic layouts (paged): block (part, i) looks at the boundary
+    // between CTA ranges i and i + 1 and handles the token set that crosses
+    // it if that set starts in range i.  Partial slots of part p are offset by
+    // p * C.
+    int s, part, c_lo, P;
     if (Geo::kStaticLayout) {
-        const int part = blockIdx.x / (C - 1);
-        const int i = blockIdx.x - part * (C - 1);
+        s = blockIdx.x;
+        part = geo.segment_part(s);
         const long long P0 = geo.part_begin(part, nullptr);
         const long long N = geo.part_tiles(part, nullptr);
         const long long Ce = min(static_cast<long long>(C), N);
+        const long long first = geo.segment_first(s) - P0;
+        const long long last = first + geo.segment_ntiles(s) - 1;
+        c_lo = static_cast<int>(((first + 1) * Ce - 1) / N);
+        const int c_hi = static_cast<int>(((last + 1) * Ce - 1) / N);
+        if (c_lo == c_hi) return;
+        P = c_hi - c_lo + 1;
+        pdl_wait();
+        geo.cta_init(gsm, nullptr, false);
+        __syncthreads();
+    } else {
+        pdl_wait();
+        geo.cta_init(gsm, nullptr, false);
+        __syncthreads();
+        part = blockIdx.x / (C - 1);
+        const int i = blockIdx.x - part * (C - 1);
+        const long long P0 = geo.part_begin(part, gsm);
+        const long long N = geo.part_tiles(part, gsm);
+        const int Ce = static_cast<int>(min(static_cast<long long>(C), N));  // CTAs with a range
         if (i >= Ce - 1) return;
         const long long start_i = P0 + N * i / Ce, tb = P0 + N * (i + 1) / Ce;
-        const long long first = geo.segment_first(geo.seg_of(tb, nullptr));
+        s = geo.seg_of(tb, gsm);
+        const long long first = geo.segment(s, gsm).first;
         if (!(first < tb && first >= start_i)) return;
+        const long long last = first + geo.segment(s, gsm).ntiles - 1 - P0;
+        c_lo = i;
+        P = static_cast<int>(((last + 1) * Ce - 1) / N) - i + 1;
     }
-    pdl_wait();
-    geo.cta_init(gsm, nullptr, false);
-    __syncthreads();
-    const int part = blockIdx.x / (C - 1);
-    const int i = blockIdx.x - part * (C - 1);
-    const long long P0 = geo.part_begin(part, gsm);
-    const long long N = geo.part_tiles(part, gsm);
-    const int Ce = static_cast<int>(min(static_cast<long long>(C), N));  // CTAs with a range
-    if (i >= Ce - 1) return;
-    const long long start_i = P0 + N * i / Ce, tb = P0 + N * (i + 1) / Ce;
-    const int s = geo.seg_of(tb, gsm);
     const Seg sg = geo.segment(s, gsm);
-    if (!(sg.first < tb && sg.first >= start_i)) return;
-    const long long last = sg.first + sg.ntiles - 1 - P0;
-    const int c_hi = static_cast<int>(((last + 1) * Ce - 1) / N);
-    const int P = c_hi - i + 1;
-    const size_t slot0 = static_cast<size_t>(i) + static_cast<size_t>(s) +
+    const size_t slot0 = static_cast<size_t>(c_lo) + static_cast<size_t>(s) +
                          static_cast<size_t>(part) * C;
 
     const int it = threadIdx.x % items, grp = threadIdx.x / items;
-    const int h = it / MERGE_ITEMS_PER_HEAD, col = it % MERGE_ITEMS_PER_HEAD;
+    const int hl = it / MERGE_ITEMS, col = it % MERGE_ITEMS;  // head within the block, column
+    const int h = blockIdx.y * hpb + hl;
     if (grp < ngrp) {
         float M = -INFINITY, L = 0.f;
         float a[MERGE_COLS];
@@ -812,9 +835,9 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
             M = mx;
         }
         if (col == 0) {
-            Mg[grp * MAXG + h] = M;
-            Lg[grp * MAXG + h] = L;
-            Bg[grp * MAXG + h] = bad;
+            Mg[grp * MAXG + hl] = M;
+            Lg[grp * MAXG + hl] = L;
+            Bg[grp * MAXG + hl] = bad;
         }
         Og[2 * (grp * items + it)] = make_float4(a[0], a[1], a[2], a[3]);
         Og[2 * (grp * items + it) + 1] = make_float4(a[4], a[5], a[6], a[7]);
@@ -824,8 +847,8 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         float M = -INFINITY;
         int bad = 0;
         for (int g2 = 0; g2 < ngrp; ++g2) {
-            M = fmaxf(M, Mg[g2 * MAXG + h]);
-            bad |= Bg[g2 * MAXG + h];
+            M = fmaxf(M, Mg[g2 * MAXG + hl]);
+            bad |= Bg[g2 * MAXG + hl];
         }
         float L = 0.f;
         float a[MERGE_COLS];
@@ -833,12 +856,12 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         for (int c = 0; c < MERGE_COLS; ++c) a[c] = 0.f;
         if (M != -INFINITY) {
             for (int g2 = 0; g2 < ngrp; ++g2) {
-                const float mg = Mg[g2 * MAXG + h];
+                const float mg = Mg[g2 * MAXG + hl];
                 if (mg == -INFINITY) continue;
                 const float e = fast_exp2(mg - M);
                 const float4 v0 = Og[2 * (g2 * items + it)];
                 const float4 v1 = Og[2 * (g2 * items + it) + 1];
-                L = fmaf(Lg[g2 * MAXG + h], e, L);
+                L = fmaf(Lg[g2 * MAXG + hl], e, L);
                 a[0] = fmaf(v0.x, e, a[0]);
                 a[1] = fmaf(v0.y, e, a[1]);
                 a[2] = fmaf(v0.z, e, a[2]);
@@ -904,7 +927,7 @@ static size_t workspace_bytes(int B, int Hq, int Hkv, int d, int num_ctas) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d != D || num_ctas < 0) return 0;
     const int G = Hq / Hkv;
     if (G > MAXG) return 0;
-    int C = num_ctas > 0 ? num_ctas : device_sm_count();
+    int C = num_ctas > 0 ? num_ctas : device_sm_count() * ATTN_CTAS_PER_SM;
     if (C <= 0) return 0;
     return partial_bytes(2ll * C + static_cast<long long>(B) * Hkv, G);
 }
@@ -933,7 +956,8 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
     if (smem > static_cast<size_t>(SMEM_LIMIT) || msmem > static_cast<size_t>(MERGE_SMEM_LIMIT))
         return CLO_ERR_UNSUPPORTED;
 
-    int C = (opts != nullptr && opts->num_ctas > 0) ? opts->num_ctas : device_sm_count();
+    int C = (opts != nullptr && opts->num_ctas > 0) ? opts->num_ctas
+                                                    : device_sm_count() * ATTN_CTAS_PER_SM;
     if (C <= 0) return CLO_ERR_CUDA;
     // Never more CTAs than tiles (no CTA gets an empty range) and at least one
     // tile per warp where the problem allows.
@@ -956,8 +980,14 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
     if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
     if (C >= 2) {
-        if (launch_pdl(attn_merge_kernel<Geo>, dim3(Geo::kParts * (C - 1)), dim3(MERGE_THREADS),
-                       msmem, stream, geo, o, C) != cudaSuccess)
+        const int merge_blocks = Geo::kStaticLayout ? geo.num_segments() : Geo::kParts * (C - 1);
+        // All heads in one block when every cut token set has few enough
+        // partials for one round of loads per thread group; else one head per block.
+        const long long most = geo.max_partials_host(C);
+        const int ngrp_all = MERGE_THREADS / (o.G * MERGE_ITEMS);
+        const int hpb = most <= static_cast<long long>(ngrp_all) * MERGE_UNROLL ? o.G : 1;
+        if (launch_pdl(attn_merge_kernel<Geo>, dim3(merge_blocks, o.G / hpb), dim3(MERGE_THREADS),
+                       msmem, stream, geo, o, C, hpb) != cudaSuccess)
             return CLO_ERR_CUDA;
     }
     return CLO_OK;
@@ -1023,6 +1053,7 @@ extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* 
     geo.n0 = static_cast<long long>(B) * Np * (Np > 0 ? geo.tp : 0);
     geo.n1 = static_cast<long long>(B) * (Hkv - Np) * (has_cb ? geo.tc : 0);
     const long long N = geo.n0 + geo.n1;
+    if (N >= (1ll << 31)) return CLO_ERR_UNSUPPORTED;  // tile counts stay 32-bit per CTA
 
     AttnOut o{};
     o.q = q;

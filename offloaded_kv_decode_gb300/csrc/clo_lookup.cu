@@ -21,7 +21,9 @@ namespace cg = cooperative_groups;
 namespace clo {
 
 constexpr int LK_CLUSTER = 8;
-constexpr int LK_THREADS = 256;
+// 4 warps per CTA: small enough (with <= 64 registers per thread) to be
+// resident next to an attention CTA, so a lookup can overlap attention.
+constexpr int LK_THREADS = 128;
 constexpr int LK_WARPS = LK_THREADS / 32;
 constexpr int LK_MAX_G = 8;
 constexpr int LK_MAX_GROUPS = 65536;
@@ -60,7 +62,7 @@ __device__ __forceinline__ float2 h2f(uint32_t v) {
     return __half22float2(h);
 }
 
-__global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS)
+__global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS, 8)
     lookup_update_kernel(const LookupParams p) {
     extern __shared__ uint8_t miss_sm[];  // miss bit of each group of this CTA
     __shared__ int cta_misses;
