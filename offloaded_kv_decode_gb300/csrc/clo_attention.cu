@@ -51,15 +51,28 @@ constexpr int KV_TILE_BYTES = TILE * ROW_BYTES;  // 4 KB of K (or V) per tile
 constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;   // K + V
 constexpr int MAXG = 8;
 constexpr int OSTRIDE = D + 4;  // padded merge-area row (floats): conflict-free writes
-constexpr int ATTN_WARPS = 4;
-constexpr int ATTN_CTAS_PER_SM = 2;
-constexpr int ATTN_STAGES = 3;
+// Shape of the main kernel (overridable at build time): warps per CTA, ring
+// stages per warp, CTAs per SM.  Shared memory per CTA is about
+// warps * stages * 8 KB plus the merge area.
+#ifndef CLO_ATTN_WARPS
+#define CLO_ATTN_WARPS 4
+#endif
+#ifndef CLO_ATTN_STAGES
+#define CLO_ATTN_STAGES 2
+#endif
+#ifndef CLO_ATTN_CTAS_PER_SM
+#define CLO_ATTN_CTAS_PER_SM 3
+#endif
+constexpr int ATTN_WARPS = CLO_ATTN_WARPS;
+constexpr int ATTN_CTAS_PER_SM = CLO_ATTN_CTAS_PER_SM;
+constexpr int ATTN_STAGES = CLO_ATTN_STAGES;
 constexpr int ATTN_THREADS = ATTN_WARPS * 32;
 constexpr int MERGE_THREADS = 512;
 constexpr int MAX_HKV_HYBRID = 64;
 constexpr int MAX_PAGED_B = 4096;
 constexpr int MAX_ROWS = 1 << 24;  // rows per head: row offsets stay 32-bit
-constexpr int SMEM_LIMIT = 113 * 1024;  // two CTAs per SM
+constexpr int SMEM_LIMIT = 227 * 1024;     // per CTA
+constexpr int SMEM_PER_SM = 228 * 1024;    // per SM, 1 KB of it reserved per resident CTA
 constexpr int MERGE_SMEM_LIMIT = 96 * 1024;
 
 // One token set: batch row (or request) b, KV head kv.
@@ -160,6 +173,25 @@ struct HybridGeo {
                           : n0 + static_cast<long long>(s - B * Np) * tc;
     }
     __device__ int segment_part(int s) const { return s < B * Np ? 0 : 1; }
+    // KV head of token set s read straight from persist_ids (no shared table);
+    // ids_ok = the ids are distinct and in range (else the slots map to heads
+    // 0..Hkv-1 in order, as in cta_init).
+    __device__ int segment_kv_direct(int s, bool& ids_ok) const {
+        unsigned long long used = 0ull;
+        ids_ok = true;
+        for (int j = 0; j < Np; ++j) {
+            const int g = __ldg(persist_ids + j);
+            if (g < 0 || g >= Hkv || ((used >> g) & 1ull)) ids_ok = false;
+            else used |= 1ull << g;
+        }
+        const int slot = s < B * Np ? s % Np : Np + (s - B * Np) % (Hkv - Np);
+        if (!ids_ok) return slot;
+        if (slot < Np) return __ldg(persist_ids + slot);
+        int left = slot - Np;
+        for (int g = 0; g < Hkv; ++g)
+            if (!((used >> g) & 1ull) && left-- == 0) return g;
+        return 0;
+    }
     // Upper bound on the CTA ranges one token set can span (host side).
     long long max_partials_host(int C) const {
         long long most = 1;
@@ -169,7 +201,7 @@ struct HybridGeo {
     }
     __device__ int segment_ntiles(int s) const { return s < B * Np ? tp : tc; }
     __host__ __device__ int num_segments() const { return B * Hkv; }
-    __device__ Seg segment(int s, const int* sm) const {
+    __device__ Seg segment(int s, const int* sm, bool no_kv = false) const {
         Seg g;
         int slot;
         if (s < B * Np) {
@@ -190,7 +222,7 @@ struct HybridGeo {
             g.first = n0 + static_cast<long long>(s1) * tc;
             g.slot = -1;
         }
-        g.kv = sm[1 + slot];
+        g.kv = no_kv ? 0 : sm[1 + slot];
         return g;
     }
     __device__ bool all_bad(const int* sm) const { return sm[0] == 0; }
@@ -215,7 +247,7 @@ struct HybridGeo {
             bk = pK + base;
             bv = pV + base;
             roff = tok * D;
-            ok = sm[0] != 0;
+            ok = true;  // slot-addressed: valid even if persist_ids is not (outputs zeroed then)
         } else {
             const long long base = (static_cast<long long>(g.b) * Hkv + g.kv) * C * D;
             bk = cbK + base;
@@ -310,11 +342,15 @@ struct PagedGeo {
     }
     __device__ long long segment_first(int) const { return 0; }  // unused: layout is dynamic
     __device__ int segment_part(int) const { return 0; }
+    __device__ int segment_kv_direct(int s, bool& ids_ok) const {
+        ids_ok = true;
+        return s % Hkv;
+    }
     // Lengths live on the device: assume the worst case (one head per block).
     long long max_partials_host(int C) const { return static_cast<long long>(C); }
     __device__ int segment_ntiles(int) const { return 0; }
     __host__ __device__ int num_segments() const { return B * Hkv; }
-    __device__ Seg segment(int s, const int* sm) const {
+    __device__ Seg segment(int s, const int* sm, bool = false) const {
         Seg g;
         g.b = s / Hkv;
         g.kv = s - g.b * Hkv;
@@ -597,9 +633,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
     pdl_wait();
-    geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
-    __syncthreads();
-    const bool all_bad = geo.all_bad(gsm);
+    // With a static layout (hybrid) the CTA ranges and the addresses of
+    // contiguous Persistent Cache tiles need no shared state, so the first of
+    // those copies are issued before the CTA reads persist_ids; the id round
+    // trip then overlaps the first data round trip.
+    constexpr bool kEarly = Geo::kStaticLayout;
+    if (!kEarly) {
+        geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
+        __syncthreads();
+    }
 
     // Every part is cut into C_p = min(C, tiles of the part) equal ranges;
     // CTA c owns range c of every part (the paged tile count is only known on
@@ -643,15 +685,38 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
         }
         prefetch_tile(geo, gsm, t, lane, cur, pd);
     };
-    cursor_init(geo, gsm, tile_at(min(static_cast<long long>(warp), total - 1)), cur);
-    cur_part1 = Geo::kParts > 1 && rl[0] == 0;
+    const long long u_first = min(static_cast<long long>(warp), total - 1);
+    int n_early = 0;
+    if (kEarly && u_first < rl[0]) {
+        cursor_init(geo, gsm, tile_at(u_first), cur);  // part 0: the table's kv is not used
+#pragma unroll
+        for (int j = 0; j < ATTN_STAGES - 1; ++j) {
+            if (n_early == j && j < nj && warp + static_cast<long long>(j) * ATTN_WARPS < rl[0]) {
+                prefetch(j);
+                issue_tile(geo, gsm, pd, ring + j * STAGE_BYTES, my_masks + j, lane, kv_policy);
+                cp_async_commit();
+                ++n_early;
+            }
+        }
+    }
+    if (kEarly) {
+        geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
+        __syncthreads();
+    }
+    const bool all_bad = geo.all_bad(gsm);
+    if (n_early == 0) {
+        cursor_init(geo, gsm, tile_at(u_first), cur);
+        cur_part1 = Geo::kParts > 1 && u_first >= rl[0];
+    }
 #pragma unroll
     for (int j = 0; j < ATTN_STAGES - 1; ++j) {
-        if (j < nj) {
-            prefetch(j);
-            issue_tile(geo, gsm, pd, ring + j * STAGE_BYTES, my_masks + j, lane, kv_policy);
+        if (j >= n_early) {
+            if (j < nj) {
+                prefetch(j);
+                issue_tile(geo, gsm, pd, ring + j * STAGE_BYTES, my_masks + j, lane, kv_policy);
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
     }
     if (ATTN_STAGES - 1 < nj) prefetch(ATTN_STAGES - 1);
 
@@ -755,8 +820,6 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         if (c_lo == c_hi) return;
         P = c_hi - c_lo + 1;
         pdl_wait();
-        geo.cta_init(gsm, nullptr, false);
-        __syncthreads();
     } else {
         pdl_wait();
         geo.cta_init(gsm, nullptr, false);
@@ -775,7 +838,26 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         c_lo = i;
         P = static_cast<int>(((last + 1) * Ce - 1) / N) - i + 1;
     }
-    const Seg sg = geo.segment(s, gsm);
+    // Output rows of the set: batch row and KV head.  With a static layout
+    // thread 0 resolves the KV head from persist_ids while the other threads
+    // load partials; it is published before the combine below.
+    __shared__ int kv_sm, ids_bad_sm;
+    int b_out;
+    if (Geo::kStaticLayout) {
+        b_out = geo.segment(s, nullptr, true).b;
+        if (threadIdx.x == 0) {
+            bool ids_ok;
+            kv_sm = geo.segment_kv_direct(s, ids_ok);
+            ids_bad_sm = ids_ok ? 0 : 1;
+        }
+    } else {
+        const Seg sg0 = geo.segment(s, gsm);
+        b_out = sg0.b;
+        if (threadIdx.x == 0) {
+            kv_sm = sg0.kv;
+            ids_bad_sm = 0;
+        }
+    }
     const size_t slot0 = static_cast<size_t>(c_lo) + static_cast<size_t>(s) +
                          static_cast<size_t>(part) * C;
 
@@ -845,7 +927,7 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
     __syncthreads();
     if (grp == 0) {
         float M = -INFINITY;
-        int bad = 0;
+        int bad = ids_bad_sm;
         for (int g2 = 0; g2 < ngrp; ++g2) {
             M = fmaxf(M, Mg[g2 * MAXG + hl]);
             bad |= Bg[g2 * MAXG + hl];
@@ -873,7 +955,7 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
             }
         }
         const bool empty = !(L > 0.f);
-        const size_t row = static_cast<size_t>(sg.b) * o.Hq + static_cast<size_t>(sg.kv) * G + h;
+        const size_t row = static_cast<size_t>(b_out) * o.Hq + static_cast<size_t>(kv_sm) * G + h;
         const float inv = (bad || empty) ? 0.f : 1.f / L;
         uint4 pk;
         __half2 h0 = __floats2half2_rn(a[0] * inv, a[1] * inv);
@@ -956,8 +1038,12 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
     if (smem > static_cast<size_t>(SMEM_LIMIT) || msmem > static_cast<size_t>(MERGE_SMEM_LIMIT))
         return CLO_ERR_UNSUPPORTED;
 
-    int C = (opts != nullptr && opts->num_ctas > 0) ? opts->num_ctas
-                                                    : device_sm_count() * ATTN_CTAS_PER_SM;
+    // As many CTAs per SM as fit, at most ATTN_CTAS_PER_SM (a large query
+    // group needs a larger merge area).
+    int per_sm = static_cast<int>(SMEM_PER_SM / (smem + 1024));
+    if (per_sm > ATTN_CTAS_PER_SM) per_sm = ATTN_CTAS_PER_SM;
+    if (per_sm < 1) return CLO_ERR_UNSUPPORTED;
+    int C = (opts != nullptr && opts->num_ctas > 0) ? opts->num_ctas : device_sm_count() * per_sm;
     if (C <= 0) return CLO_ERR_CUDA;
     // Never more CTAs than tiles (no CTA gets an empty range) and at least one
     // tile per warp where the problem allows.
