@@ -60,6 +60,9 @@ constexpr int OSTRIDE = D + 4;  // padded merge-area row (floats): conflict-free
 #ifndef CLO_ATTN_STAGES
 #define CLO_ATTN_STAGES 2
 #endif
+#ifndef CLO_ATTN_REVERSE_ODD
+#define CLO_ATTN_REVERSE_ODD 1
+#endif
 #ifndef CLO_ATTN_CTAS_PER_SM
 #define CLO_ATTN_CTAS_PER_SM 3
 #endif
@@ -123,9 +126,17 @@ struct HybridGeo {
     // [1 + Hkv .. 1 + 2 Hkv) staged persist_ids.
     static size_t smem_ints(int Hkv_, int /*B*/) { return 2 * static_cast<size_t>(Hkv_) + 4; }
 
+    // This thread's share of persist_ids (thread j < Np loads entry j); issued
+    // ahead of the bulk copies so it does not queue behind them.
+    __device__ int ids_preload() const {
+        return static_cast<int>(threadIdx.x) < Np ? __ldg(persist_ids + threadIdx.x) : 0;
+    }
     __device__ void cta_init(int* sm, int32_t* err_flag, bool report) const {
+        cta_init_with(sm, err_flag, report, ids_preload());
+    }
+    __device__ void cta_init_with(int* sm, int32_t* err_flag, bool report, int id) const {
         // sm[1 + Hkv + j] stages persist_ids so thread 0 does not wait on Np loads in turn.
-        if (static_cast<int>(threadIdx.x) < Np) sm[1 + Hkv + threadIdx.x] = persist_ids[threadIdx.x];
+        if (static_cast<int>(threadIdx.x) < Np) sm[1 + Hkv + threadIdx.x] = id;
         __syncthreads();
         if (threadIdx.x == 0) {
             unsigned long long used = 0ull;
@@ -638,7 +649,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     // those copies are issued before the CTA reads persist_ids; the id round
     // trip then overlaps the first data round trip.
     constexpr bool kEarly = Geo::kStaticLayout;
-    if (!kEarly) {
+    int ids_pre = 0;
+    if constexpr (kEarly) {
+        ids_pre = geo.ids_preload();
+    } else {
         geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
         __syncthreads();
     }
@@ -663,10 +677,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
         total += rl[p];
     }
     if (total == 0) return;  // uniform over the CTA
-
-    // Warp w takes the CTA's tiles w, w + 8, ... of the concatenated ranges.
+    // Odd CTAs take their two ranges in the opposite order, so that half the
+    // grid reads scattered Cache Buffer rows while the other half streams
+    // the Persistent Cache: the part switch is not taken by every CTA at
+    // once (a grid-wide switch stalls the memory pipeline while every warp
+    // flushes its segment and waits on its first scattered tile).
+    const int pf = (Geo::kParts > 1 && CLO_ATTN_REVERSE_ODD && (blockIdx.x & 1)) ? 1 : 0;
+    const int ps = Geo::kParts - 1 - pf;
+    // Warp w takes the CTA's tiles w, w + ATTN_WARPS, ... of the concatenated ranges.
     auto tile_at = [&](long long u) -> long long {
-        return u < rl[0] ? ra[0] + u : ra[Geo::kParts - 1] + (u - rl[0]);
+        return u < rl[pf] ? ra[pf] + u : ra[ps] + (u - rl[pf]);
     };
     const int nj = warp < total ? static_cast<int>((total - warp + ATTN_WARPS - 1) / ATTN_WARPS) : 0;
     const uint32_t ring = smem_u32(smem) + warp * ATTN_STAGES * STAGE_BYTES;
@@ -674,20 +694,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
 
     const uint64_t kv_policy = l2_evict_first_policy();
     Cursor cur;
-    bool cur_part1 = false;
+    bool switched = false;
     Pending pd;
     auto prefetch = [&](int j) {
         const long long u = warp + static_cast<long long>(j) * ATTN_WARPS;
         const long long t = tile_at(u);
-        if (Geo::kParts > 1 && u >= rl[0] && !cur_part1) {
-            cursor_init(geo, gsm, t, cur);  // jump to this CTA's range of part 1
-            cur_part1 = true;
+        if (Geo::kParts > 1 && u >= rl[pf] && !switched) {
+            cursor_init(geo, gsm, t, cur);  // jump to this CTA's range of the other part
+            switched = true;
         }
         prefetch_tile(geo, gsm, t, lane, cur, pd);
     };
     const long long u_first = min(static_cast<long long>(warp), total - 1);
     int n_early = 0;
-    if (kEarly && u_first < rl[0]) {
+    if (kEarly && pf == 0 && u_first < rl[0]) {
         cursor_init(geo, gsm, tile_at(u_first), cur);  // part 0: the table's kv is not used
 #pragma unroll
         for (int j = 0; j < ATTN_STAGES - 1; ++j) {
@@ -699,14 +719,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
             }
         }
     }
-    if (kEarly) {
-        geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
+    if constexpr (kEarly) {
+        geo.cta_init_with(gsm, o.err_flag, blockIdx.x == 0, ids_pre);
         __syncthreads();
     }
     const bool all_bad = geo.all_bad(gsm);
     if (n_early == 0) {
         cursor_init(geo, gsm, tile_at(u_first), cur);
-        cur_part1 = Geo::kParts > 1 && u_first >= rl[0];
+        switched = Geo::kParts > 1 && u_first >= rl[pf];
     }
 #pragma unroll
     for (int j = 0; j < ATTN_STAGES - 1; ++j) {
@@ -723,7 +743,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     int jc = 0;
     WarpState w;
 #pragma unroll 1
-    for (int p = 0; p < Geo::kParts; ++p) {
+    for (int pi = 0; pi < Geo::kParts; ++pi) {
+        const int p = pi == 0 ? pf : ps;
         if (rl[p] == 0) continue;
         const long long c0 = ra[p], c1 = ra[p] + rl[p];
         const int s_first = geo.seg_of(c0, gsm), s_last = geo.seg_of(c1 - 1, gsm);
@@ -736,7 +757,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
             state_reset(w);
             while (jc < nj) {
                 const long long t = tile_at(warp + static_cast<long long>(jc) * ATTN_WARPS);
-                if (t >= seg_end) break;
+                if (t >= seg_end || t < sg.first) break;  // (a reversed CTA goes back to part 0)
                 cp_async_wait<ATTN_STAGES - 2>();
                 __syncwarp();
                 const int jn = jc + ATTN_STAGES - 1;
