@@ -184,20 +184,28 @@ struct HybridGeo {
                           : n0 + static_cast<long long>(s - B * Np) * tc;
     }
     __device__ int segment_part(int s) const { return s < B * Np ? 0 : 1; }
-    // KV head of token set s read straight from persist_ids (no shared table);
-    // ids_ok = the ids are distinct and in range (else the slots map to heads
-    // 0..Hkv-1 in order, as in cta_init).
-    __device__ int segment_kv_direct(int s, bool& ids_ok) const {
-        unsigned long long used = 0ull;
-        ids_ok = true;
-        for (int j = 0; j < Np; ++j) {
-            const int g = __ldg(persist_ids + j);
-            if (g < 0 || g >= Hkv || ((used >> g) & 1ull)) ids_ok = false;
-            else used |= 1ull << g;
-        }
+    // KV head of token set s from persist_ids, computed by one warp without
+    // a shared table: lane j holds entries j and j + 32 (-1 past Np, loaded
+    // with ids_warp_load).  ids_ok = the ids are distinct and in range (else
+    // the slots map to heads 0..Hkv-1 in order, as in cta_init).
+    __device__ void ids_warp_load(int lane, int& id0, int& id1) const {
+        id0 = lane < Np ? __ldg(persist_ids + lane) : -1;
+        id1 = lane + 32 < Np ? __ldg(persist_ids + lane + 32) : -1;
+    }
+    __device__ int segment_kv_warp(int s, int lane, int id0, int id1, bool& ids_ok) const {
+        const bool in0 = lane < Np, in1 = lane + 32 < Np;
+        const bool bad = (in0 && (id0 < 0 || id0 >= Hkv)) || (in1 && (id1 < 0 || id1 >= Hkv));
+        unsigned long long mine = 0ull;
+        if (in0 && !bad) mine |= 1ull << id0;
+        if (in1 && !bad) mine |= 1ull << id1;
+        const unsigned lo = __reduce_or_sync(FULL_MASK, static_cast<unsigned>(mine));
+        const unsigned hi = __reduce_or_sync(FULL_MASK, static_cast<unsigned>(mine >> 32));
+        const unsigned long long used = (static_cast<unsigned long long>(hi) << 32) | lo;
+        ids_ok = !__any_sync(FULL_MASK, bad) && __popcll(used) == Np;  // no duplicates
         const int slot = s < B * Np ? s % Np : Np + (s - B * Np) % (Hkv - Np);
+        const int own = __shfl_sync(FULL_MASK, slot < 32 ? id0 : id1, slot & 31);
         if (!ids_ok) return slot;
-        if (slot < Np) return __ldg(persist_ids + slot);
+        if (slot < Np) return own;
         int left = slot - Np;
         for (int g = 0; g < Hkv; ++g)
             if (!((used >> g) & 1ull) && left-- == 0) return g;
@@ -353,10 +361,6 @@ struct PagedGeo {
     }
     __device__ long long segment_first(int) const { return 0; }  // unused: layout is dynamic
     __device__ int segment_part(int) const { return 0; }
-    __device__ int segment_kv_direct(int s, bool& ids_ok) const {
-        ids_ok = true;
-        return s % Hkv;
-    }
     // Lengths live on the device: assume the worst case (one head per block).
     long long max_partials_host(int C) const { return static_cast<long long>(C); }
     __device__ int segment_ntiles(int) const { return 0; }
@@ -860,17 +864,17 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         P = static_cast<int>(((last + 1) * Ce - 1) / N) - i + 1;
     }
     // Output rows of the set: batch row and KV head.  With a static layout
-    // thread 0 resolves the KV head from persist_ids while the other threads
-    // load partials; it is published before the combine below.
+    // the last warp loads persist_ids now and resolves the KV head once its
+    // partials are in; it is published before the combine below.
     __shared__ int kv_sm, ids_bad_sm;
     int b_out;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kIdsWarp = MERGE_THREADS / 32 - 1;
+    int id0 = -1, id1 = -1;
     if (Geo::kStaticLayout) {
         b_out = geo.segment(s, nullptr, true).b;
-        if (threadIdx.x == 0) {
-            bool ids_ok;
-            kv_sm = geo.segment_kv_direct(s, ids_ok);
-            ids_bad_sm = ids_ok ? 0 : 1;
-        }
+        if constexpr (Geo::kStaticLayout)
+            if (warp == kIdsWarp) geo.ids_warp_load(lane, id0, id1);
     } else {
         const Seg sg0 = geo.segment(s, gsm);
         b_out = sg0.b;
@@ -885,12 +889,12 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
     const int it = threadIdx.x % items, grp = threadIdx.x / items;
     const int hl = it / MERGE_ITEMS, col = it % MERGE_ITEMS;  // head within the block, column
     const int h = blockIdx.y * hpb + hl;
-    if (grp < ngrp) {
-        float M = -INFINITY, L = 0.f;
-        float a[MERGE_COLS];
+    float M = -INFINITY, L = 0.f;
+    float a[MERGE_COLS];
 #pragma unroll
-        for (int c = 0; c < MERGE_COLS; ++c) a[c] = 0.f;
-        int bad = 0;
+    for (int c = 0; c < MERGE_COLS; ++c) a[c] = 0.f;
+    int bad = 0;
+    if (grp < ngrp) {
         for (int p0 = grp; p0 < P; p0 += MERGE_UNROLL * ngrp) {
             float x[MERGE_UNROLL];
             float4 v0[MERGE_UNROLL], v1[MERGE_UNROLL];
@@ -945,36 +949,55 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         Og[2 * (grp * items + it)] = make_float4(a[0], a[1], a[2], a[3]);
         Og[2 * (grp * items + it) + 1] = make_float4(a[4], a[5], a[6], a[7]);
     }
-    __syncthreads();
-    if (grp == 0) {
-        float M = -INFINITY;
-        int bad = ids_bad_sm;
-        for (int g2 = 0; g2 < ngrp; ++g2) {
-            M = fmaxf(M, Mg[g2 * MAXG + hl]);
-            bad |= Bg[g2 * MAXG + hl];
-        }
-        float L = 0.f;
-        float a[MERGE_COLS];
-#pragma unroll
-        for (int c = 0; c < MERGE_COLS; ++c) a[c] = 0.f;
-        if (M != -INFINITY) {
-            for (int g2 = 0; g2 < ngrp; ++g2) {
-                const float mg = Mg[g2 * MAXG + hl];
-                if (mg == -INFINITY) continue;
-                const float e = fast_exp2(mg - M);
-                const float4 v0 = Og[2 * (g2 * items + it)];
-                const float4 v1 = Og[2 * (g2 * items + it) + 1];
-                L = fmaf(Lg[g2 * MAXG + hl], e, L);
-                a[0] = fmaf(v0.x, e, a[0]);
-                a[1] = fmaf(v0.y, e, a[1]);
-                a[2] = fmaf(v0.z, e, a[2]);
-                a[3] = fmaf(v0.w, e, a[3]);
-                a[4] = fmaf(v1.x, e, a[4]);
-                a[5] = fmaf(v1.y, e, a[5]);
-                a[6] = fmaf(v1.z, e, a[6]);
-                a[7] = fmaf(v1.w, e, a[7]);
+    if constexpr (Geo::kStaticLayout) {
+        if (warp == kIdsWarp) {
+            bool ids_ok;
+            const int kv = geo.segment_kv_warp(s, lane, id0, id1, ids_ok);
+            if (lane == 0) {
+                kv_sm = kv;
+                ids_bad_sm = ids_ok ? 0 : 1;
             }
         }
+    }
+    __syncthreads();
+    // Tree over the thread groups: at each level group g < n - half takes in
+    // group g + half (a fixed order, so the result does not depend on timing).
+    for (int n = ngrp; n > 1;) {
+        const int half = (n + 1) >> 1;
+        if (grp < n - half) {
+            const int q2 = grp + half;
+            const float m2 = Mg[q2 * MAXG + hl];
+            bad |= Bg[q2 * MAXG + hl];
+            const float mx = fmaxf(M, m2);
+            if (mx != -INFINITY) {
+                const float e1 = fast_exp2(M - mx), e2 = fast_exp2(m2 - mx);
+                const float4 w0 = Og[2 * (q2 * items + it)], w1 = Og[2 * (q2 * items + it) + 1];
+                L = L * e1 + Lg[q2 * MAXG + hl] * e2;
+                a[0] = fmaf(w0.x, e2, a[0] * e1);
+                a[1] = fmaf(w0.y, e2, a[1] * e1);
+                a[2] = fmaf(w0.z, e2, a[2] * e1);
+                a[3] = fmaf(w0.w, e2, a[3] * e1);
+                a[4] = fmaf(w1.x, e2, a[4] * e1);
+                a[5] = fmaf(w1.y, e2, a[5] * e1);
+                a[6] = fmaf(w1.z, e2, a[6] * e1);
+                a[7] = fmaf(w1.w, e2, a[7] * e1);
+                M = mx;
+            }
+            if (half > 1) {
+                if (col == 0) {
+                    Mg[grp * MAXG + hl] = M;
+                    Lg[grp * MAXG + hl] = L;
+                    Bg[grp * MAXG + hl] = bad;
+                }
+                Og[2 * (grp * items + it)] = make_float4(a[0], a[1], a[2], a[3]);
+                Og[2 * (grp * items + it) + 1] = make_float4(a[4], a[5], a[6], a[7]);
+            }
+        }
+        __syncthreads();
+        n = half;
+    }
+    if (grp == 0) {
+        bad |= ids_bad_sm;
         const bool empty = !(L > 0.f);
         const size_t row = static_cast<size_t>(b_out) * o.Hq + static_cast<size_t>(kv_sm) * G + h;
         const float inv = (bad || empty) ? 0.f : 1.f / L;
