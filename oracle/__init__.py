@@ -69,6 +69,9 @@ class Oracle:
         lib.oracle_paged_attn.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
                                           _I, _I, _D, _P, _P]
         lib.oracle_paged_attn.restype = _I
+        lib.oracle_fill_cache_buffer.argtypes = [_P, _P, _I, _P, _P, _I, _P, _P, _I,
+                                                 _P, _I, _I, _I, _I]
+        lib.oracle_fill_cache_buffer.restype = _I
         self.lib = lib
 
     # -- helpers ----------------------------------------------------------
@@ -187,6 +190,27 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"oracle_paged_attn rc={rc}")
         return out, lse
+
+    def fill_cache_buffer(self, srcK, srcV, tok, slot, cbK, cbV, miss_list):
+        """Miss-path fill.  srcK/srcV [B][Hkv][T][d], tok/slot [B][Hkv][k]
+        (slot None: token-addressed), cbK/cbV [B][Hkv][C][d] (not modified;
+        filled copies are returned), miss_list [n] -> (cbK, cbV, rc) with rc
+        0 or BAD_INDEX."""
+        srcK, srcV = self._u16(srcK), self._u16(srcV)
+        outK, outV = self._u16(cbK).copy(), self._u16(cbV).copy()
+        tok = self._i32(tok)
+        sl = None if slot is None else self._i32(slot)
+        ml = self._i32(miss_list).ravel()
+        B, Hkv, T, d = srcK.shape
+        C = outK.shape[2]
+        k = tok.shape[2]
+        rc = self.lib.oracle_fill_cache_buffer(
+            _ptr(srcK), _ptr(srcV), T, _ptr(tok), None if sl is None else _ptr(sl), k,
+            _ptr(outK), _ptr(outV), C, _ptr(ml) if ml.size else None, int(ml.size),
+            B, Hkv, d)
+        if rc not in (OK, BAD_INDEX):
+            raise ValueError(f"oracle_fill_cache_buffer rc={rc}")
+        return outK, outV, rc
 
 
 _default = None

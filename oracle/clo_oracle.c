@@ -30,6 +30,13 @@
  *                         for Online LLM Inference", method details, system
  *                         implementation and CPU kernel (vLLM-like paged KV
  *                         cache, one decode query per request); same attention.
+ *   oracle_fill_cache_buffer  CLO page, section 3, Fig. 7 (an update writes
+ *                         the new KV data straight to its final position, no
+ *                         staging buffer) and section 2 (only missed heads
+ *                         are transferred): for every KV head on the miss
+ *                         list, copy the rows of its new top-k token set from
+ *                         the full KV copy into the Cache Buffer rows that
+ *                         the hybrid attention reads.
  *
  * Readings where the pages are silent:
  *   - GQA grouping is contiguous: query head h belongs to KV head h / G.
@@ -40,6 +47,9 @@
  *   - sim == tau counts as a hit.
  *   - Persistent KV heads are not looked up: flag 2, labels untouched.
  *   - An empty token set gives output 0 and lse = -inf.
+ *   - The final position of a filled row is the Cache Buffer row that the
+ *     attention's index names for it; with token-addressed buffers that row
+ *     is the token itself.
  */
 #include <math.h>
 #include <stdint.h>
@@ -295,5 +305,41 @@ int oracle_paged_attn(const uint16_t* q, const uint16_t* kc, const uint16_t* vc,
         }
     }
     free(K); free(V);
+    return rc;
+}
+
+/* Miss-path fill of the Cache Buffer.
+ *   srcK/srcV  [B][Hkv][T][d]  full KV copy of every head
+ *   tok        [B][Hkv][k]     token of the j-th row of each head's new set
+ *   slot       [B][Hkv][k]     its final row in the Cache Buffer; NULL means
+ *                              the row is the token itself
+ *   cbK/cbV    [B][Hkv][C][d]  Cache Buffer, written in place
+ *   miss_list  [miss_count]    entries b * Hkv + g, one per missed KV head
+ * Every row of a listed head is copied; rows of heads not on the list and
+ * rows not selected are left as they are.  List entries outside [0, B*Hkv),
+ * tokens outside [0, T) and slots outside [0, C) are skipped, the rest is
+ * still done, and the call returns ORACLE_BAD_INDEX. */
+int oracle_fill_cache_buffer(const uint16_t* srcK, const uint16_t* srcV, int T,
+                             const int32_t* tok, const int32_t* slot, int k,
+                             uint16_t* cbK, uint16_t* cbV, int C,
+                             const int32_t* miss_list, int miss_count, int B,
+                             int Hkv, int d) {
+    if (B < 0 || Hkv <= 0 || d <= 0 || T < 0 || k < 0 || C < 0 || miss_count < 0)
+        return ORACLE_BAD_ARG;
+    int rc = ORACLE_OK;
+    for (int m = 0; m < miss_count; ++m) {
+        int e = miss_list[m];
+        if (e < 0 || e >= B * Hkv) { rc = ORACLE_BAD_INDEX; continue; }
+        for (int j = 0; j < k; ++j) {
+            size_t sel = (size_t)e * k + j;
+            int t = tok[sel];
+            int r = slot ? slot[sel] : t;
+            if (t < 0 || t >= T || r < 0 || r >= C) { rc = ORACLE_BAD_INDEX; continue; }
+            size_t from = ((size_t)e * T + t) * d;
+            size_t to = ((size_t)e * C + r) * d;
+            memcpy(cbK + to, srcK + from, (size_t)d * sizeof(uint16_t));
+            memcpy(cbV + to, srcV + from, (size_t)d * sizeof(uint16_t));
+        }
+    }
     return rc;
 }

@@ -419,6 +419,130 @@ def pin_paged_identity_and_empty(orc):
     assert np.all(out[1] == 0.0) and np.all(np.isneginf(lse[1]))
 
 
+# -- miss-path fill (CLO page, section 3, Fig. 7: new KV rows go straight to
+#    their final position; section 2: only missed heads are transferred) ------
+
+def _h(vals):
+    return np.asarray(vals, dtype=np.float16)
+
+
+def pin_fill_worked_example(orc):
+    """A case small enough to write the answer out by hand."""
+    # Full KV of B=1 batch row, 2 KV heads, T=3 tokens, d=2: K row (g, t) is
+    # [10g + t, -(10g + t)], V row is [100 + 10g + t, 0.5].
+    srcK = _h([[[[0, -0], [1, -1], [2, -2]], [[10, -10], [11, -11], [12, -12]]]])
+    srcV = _h([[[[100, .5], [101, .5], [102, .5]], [[110, .5], [111, .5], [112, .5]]]])
+    tok = np.array([[[2, 0], [1, 2]]], dtype=np.int32)
+    zero = np.zeros((1, 2, 3, 2), dtype=np.float16)
+    # Token-addressed (slot = token), only head 1 on the miss list.
+    K, V, rc = orc.fill_cache_buffer(srcK, srcV, tok, None, zero, zero, [1])
+    assert rc == 0
+    wantK = _h([[[[0, 0], [0, 0], [0, 0]], [[0, 0], [11, -11], [12, -12]]]])
+    wantV = _h([[[[0, 0], [0, 0], [0, 0]], [[0, 0], [111, .5], [112, .5]]]])
+    assert np.array_equal(K.view(np.float16), wantK), K.view(np.float16)
+    assert np.array_equal(V.view(np.float16), wantV), V.view(np.float16)
+    # Compact (slot = position in the set), both heads missed, C = 2.
+    zero2 = np.zeros((1, 2, 2, 2), dtype=np.float16)
+    slot = np.array([[[0, 1], [0, 1]]], dtype=np.int32)
+    K, V, rc = orc.fill_cache_buffer(srcK, srcV, tok, slot, zero2, zero2, [0, 1])
+    assert rc == 0
+    wantK = _h([[[[2, -2], [0, -0]], [[11, -11], [12, -12]]]])
+    wantV = _h([[[[102, .5], [100, .5]], [[111, .5], [112, .5]]]])
+    assert np.array_equal(K.view(np.float16), wantK), K.view(np.float16)
+    assert np.array_equal(V.view(np.float16), wantV), V.view(np.float16)
+
+
+def _fill_case(seed, B=2, Hkv=3, T=29, k=7, d=16, compact=False):
+    rng = _rng(seed)
+    srcK, srcV = _f16(rng, (B, Hkv, T, d)), _f16(rng, (B, Hkv, T, d))
+    tok = np.stack([rng.choice(T, k, replace=False) for _ in range(B * Hkv)])
+    tok = tok.reshape(B, Hkv, k).astype(np.int32)
+    if compact:
+        C = k
+        slot = np.stack([rng.permutation(k) for _ in range(B * Hkv)]).reshape(B, Hkv, k)
+        slot = slot.astype(np.int32)
+    else:
+        C, slot = T, None
+    cbK, cbV = _f16(rng, (B, Hkv, C, d)), _f16(rng, (B, Hkv, C, d))
+    return srcK, srcV, tok, slot, cbK, cbV
+
+
+def pin_fill_then_attention_vs_sdpa(orc):
+    """After every head is filled, the hybrid attention over the Cache Buffer
+    (rows named by the slots) equals torch SDPA over the selected rows of the
+    full KV copy: the rows landed where the attention reads them."""
+    for compact in (False, True):
+        B, Hkv, G, d = 2, 3, 2, 16
+        srcK, srcV, tok, slot, cbK, cbV = _fill_case(11 + compact, B=B, Hkv=Hkv, d=d,
+                                                     compact=compact)
+        K, V, rc = orc.fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV,
+                                         np.arange(B * Hkv))
+        assert rc == 0
+        q = _f16(_rng(5), (B, Hkv * G, d))
+        idx = tok if slot is None else slot
+        empty = np.zeros((B, 0, 1, d), dtype=np.float16)
+        out, _ = orc.hybrid_attn(q, K, V, idx, empty, empty, [], 1.0 / math.sqrt(d))
+        for b in range(B):
+            for g in range(Hkv):
+                ref = _sdpa64(q[b, g * G:(g + 1) * G], srcK[b, g, tok[b, g]],
+                              srcV[b, g, tok[b, g]], 1.0 / math.sqrt(d))
+                assert np.allclose(out[b, g * G:(g + 1) * G], ref, atol=1e-12, rtol=0), (b, g)
+
+
+def pin_fill_leaves_the_rest(orc):
+    """Heads not on the miss list, and rows not selected, keep their bytes."""
+    srcK, srcV, tok, slot, cbK, cbV = _fill_case(21)
+    B, Hkv, T = tok.shape[0], tok.shape[1], srcK.shape[2]
+    miss = [0 * Hkv + 2, 1 * Hkv + 0]
+    K, V, rc = orc.fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, miss)
+    assert rc == 0
+    cbK16, cbV16 = cbK.view(np.uint16), cbV.view(np.uint16)
+    sK, sV = srcK.view(np.uint16), srcV.view(np.uint16)
+    for b in range(B):
+        for g in range(Hkv):
+            chosen = set(tok[b, g].tolist()) if (b * Hkv + g) in miss else set()
+            for t in range(T):
+                wantK = sK[b, g, t] if t in chosen else cbK16[b, g, t]
+                wantV = sV[b, g, t] if t in chosen else cbV16[b, g, t]
+                assert np.array_equal(K[b, g, t], wantK), (b, g, t)
+                assert np.array_equal(V[b, g, t], wantV), (b, g, t)
+
+
+def pin_fill_bad_entries_skipped(orc):
+    """Out-of-range list entries, tokens and slots are skipped and reported;
+    every valid row is still written."""
+    srcK, srcV, tok, slot, cbK, cbV = _fill_case(31, compact=True)
+    B, Hkv, k = tok.shape
+    tok = tok.copy()
+    slot = slot.copy()
+    tok[0, 1, 3] = srcK.shape[2]      # token past the end
+    slot[1, 2, 0] = -1                # slot before the start
+    good = [0 * Hkv + 1, 1 * Hkv + 2]
+    K, V, rc = orc.fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, good + [B * Hkv, -3])
+    assert rc == 4
+    Kg, Vg, rcg = orc.fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, good)
+    assert rcg == 4 and np.array_equal(K, Kg) and np.array_equal(V, Vg)
+    # The skipped rows kept their old contents; the others hold the new rows.
+    for (b, g) in ((0, 1), (1, 2)):
+        for j in range(k):
+            bad = (b, g, j) in ((0, 1, 3), (1, 2, 0))
+            r = slot[b, g, j]
+            if bad:
+                continue
+            assert np.array_equal(K[b, g, r], srcK.view(np.uint16)[b, g, tok[b, g, j]])
+    assert np.array_equal(K[0, 1, slot[0, 1, 3]], cbK.view(np.uint16)[0, 1, slot[0, 1, 3]])
+
+
+def pin_fill_list_order(orc):
+    """The order of the miss list does not matter (the heads are disjoint)."""
+    srcK, srcV, tok, slot, cbK, cbV = _fill_case(41, compact=True)
+    n = tok.shape[0] * tok.shape[1]
+    a = orc.fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, np.arange(n))
+    b = orc.fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, np.arange(n)[::-1])
+    assert a[2] == b[2] == 0
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

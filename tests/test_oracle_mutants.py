@@ -44,6 +44,13 @@ MUTANTS = [
     ("binary16 exponent bias", "v = ldexp((double)(1024 + m), e - 25);",
      "v = ldexp((double)(1024 + m), e - 24);"),
     ("binary16 subnormal scale", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    ("fill slot ignored", "int r = slot ? slot[sel] : t;", "int r = t;"),
+    ("fill K from V", "memcpy(cbK + to, srcK + from,", "memcpy(cbK + to, srcV + from,"),
+    ("fill miss list ignored", "int e = miss_list[m];", "int e = m;"),
+    ("fill source row by position", "size_t from = ((size_t)e * T + t) * d;",
+     "size_t from = ((size_t)e * T + j) * d;"),
+    ("fill last row dropped", "for (int j = 0; j < k; ++j) {\n            size_t sel",
+     "for (int j = 0; j < k - 1; ++j) {\n            size_t sel"),
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
