@@ -297,6 +297,119 @@ class PagedWorkload:
                 "l2": f"inputs larger than L2: {self.bytes_per_step() / 2**30:.2f} GiB read per step"}
 
 
+class FillWorkload:
+    """Miss-path fill: every non-persistent KV head of the base layer missed,
+    its top-k rows copied from the full KV copy (pinned host memory or HBM)
+    into the Cache Buffer.  Two buffer sets (source, selection, destination)
+    alternate, so consecutive steps touch disjoint rows."""
+    kind = "fill"
+    kernel = "fill_kernel"
+    kernel_src = "clo_fill.cu"
+
+    def __init__(self, name, dev, rank: int, batch: int = 0):
+        import torch
+        import offloaded_kv_decode_gb300 as clo
+
+        base, self.src_where = wl.FILL_CONFIGS[name]
+        self.name = name
+        self.clo, self.torch = clo, torch
+        cfg = wl.CONFIGS[base]
+        if batch:
+            cfg = dataclasses.replace(cfg, B=batch)
+        self.cfg = cfg if rank == 0 else dataclasses.replace(cfg, seed=cfg.seed + 1000 * rank)
+        self.L = 1
+        self.n_inst = 2
+        self.phases = 2
+        pm = wl.persist_mask(self.cfg, 0)
+        miss = [b * cfg.Hkv + g for b in range(cfg.B) for g in range(cfg.Hkv) if not pm[g]]
+        self.n_miss = len(miss)
+        self.miss = torch.tensor(miss, dtype=torch.int32, device=dev)
+        self.count = torch.tensor([len(miss)], dtype=torch.int32, device=dev)
+        self.inst = []
+        for i in range(self.n_inst):
+            li = i + 1000 * rank
+            sK, sV = wl.full_kv(self.cfg, li, dev)
+            if self.src_where == "host":
+                sK, sV = sK.cpu().pin_memory(), sV.cpu().pin_memory()
+            tok, slot = wl.fill_selection(self.cfg, li, dev)
+            shape = (cfg.B, cfg.Hkv, cfg.C, cfg.d)
+            self.inst.append(dict(srcK=sK, srcV=sV, tok=tok, slot=slot,
+                                  cbK=torch.zeros(shape, dtype=torch.float16, device=dev),
+                                  cbV=torch.zeros(shape, dtype=torch.float16, device=dev)))
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.row_bytes = cfg.d * HALF
+
+    def link_bytes(self) -> int:
+        """K and V rows read from the full copy by one call."""
+        return self.n_miss * self.cfg.k * 2 * self.row_bytes
+
+    def bytes_per_step(self) -> int:
+        return self.link_bytes()
+
+    def attn_bytes_per_launch(self) -> int:
+        """Bytes the kernel moves through its bound: the rows read over the
+        host link, or read and written in HBM (plus the token and slot ids)."""
+        ids = self.n_miss * self.cfg.k * 8
+        if self.src_where == "host":
+            return self.link_bytes()
+        return 2 * self.link_bytes() + ids
+
+    def launches_per_step(self) -> int:
+        return 1
+
+    def launch(self, step: int, attn_events=None):
+        it = self.inst[step % self.n_inst]
+        self.clo.clo_fill_cache_buffer(it["srcK"], it["srcV"], it["tok"], it["slot"], it["cbK"],
+                                       it["cbV"], self.miss, self.count, err_flag=self.err,
+                                       events=None if attn_events is None else attn_events[0])
+
+    def roofline_peak(self):
+        """(peak GB/s, source, bound)."""
+        if self.src_where == "device":
+            p, src = peak_hbm()
+            return p, src, "hbm"
+        return measure_h2d_gbs(self.torch), "measured in this run: pinned host-to-device " \
+            "cudaMemcpyAsync of 512 MiB, best of 5", "c2c"
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.h_miss = self.miss.cpu().pin_memory()
+        self.h_count = self.count.cpu().pin_memory()
+        self.h_err = torch.zeros(1, dtype=torch.int32).pin_memory()
+        self.e2e_h2d = (self.miss.numel() + 1) * 4
+        self.e2e_d2h = 4
+
+    def e2e_step(self, step: int):
+        self.miss.copy_(self.h_miss, non_blocking=True)
+        self.count.copy_(self.h_count, non_blocking=True)
+        self.launch(step)
+        self.h_err.copy_(self.err, non_blocking=True)
+
+    def config(self) -> dict:
+        c = self.cfg
+        return {"workload": self.name, "base": c.name, "batch": c.B, "kv_heads": c.Hkv,
+                "head_dim": c.d, "context": c.T, "top_k": c.k, "missed_heads": self.n_miss,
+                "source": ("full KV copy in pinned host memory, read by the GPU over the host link"
+                           if self.src_where == "host" else "full KV copy in HBM"),
+                "rows_per_call": self.n_miss * c.k,
+                "l2": "two buffer sets alternate; consecutive calls read and write disjoint rows"}
+
+
+def measure_h2d_gbs(torch, nbytes: int = 512 * 2 ** 20, reps: int = 5) -> float:
+    """Pinned host-to-device copy bandwidth (GB/s), best of reps."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return best
+
+
 # ---------------------------------------------------------------- CPU oracle sample
 
 def oracle_sample(name: str):
@@ -340,6 +453,25 @@ def oracle_sample(name: str):
                          n * small.d * HALF * 2 + extra + 2 * G * small.d * HALF))
         desc = (f"one batch row of {cfg.name} (all {cfg.Hkv} KV heads: lookup, then attention "
                 f"over {cfg.Np} persistent x {cfg.T} and {cfg.Hkv - cfg.Np} x {cfg.k} indexed rows)")
+    elif name in wl.FILL_CONFIGS:
+        base, _ = wl.FILL_CONFIGS[name]
+        cfg = wl.CONFIGS[base]
+        small = dataclasses.replace(cfg, B=1)
+        srcK, srcV = wl.full_kv(small, 0)
+        tok, slot = wl.fill_selection(small, 0)
+        # Written once so the timed fills do not pay first-touch page faults.
+        cbK = np.full((small.B, small.Hkv, small.C, small.d), 1.0, np.float16)
+        cbV = np.full_like(cbK, 1.0)
+        pm = wl.persist_mask(small, 0)
+        sK, sV, tk, sl = srcK.numpy(), srcV.numpy(), tok.numpy(), slot.numpy()
+        for g in range(small.Hkv):
+            if pm[g]:
+                continue
+            jobs.append((lambda g=g: orc.fill_cache_buffer(sK, sV, tk, sl, cbK, cbV, [g],
+                                                           inplace=True),
+                         small.k * small.d * HALF * 2))
+        desc = (f"one batch row of {name} ({int((pm == 0).sum())} missed KV heads x {small.k} "
+                f"rows, full KV copy in host memory)")
     else:
         pc = wl.PAGED_CONFIGS[name]
         small = wl.PagedConfig(pc.name, B=4, Hq=pc.Hq, Hkv=pc.Hkv, ctx_lo=pc.ctx_lo,
@@ -436,12 +568,12 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profiles(kernel_file: str, workload: str):
+def traffic_from_profiles(kernel_file: str, kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source; else None."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", f"attn_split_kernel_{workload}.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         text = open(path).read()
     except OSError:
@@ -510,6 +642,8 @@ def run_ours(args):
         if args.batch:
             cfg = dataclasses.replace(cfg, B=args.batch)
         W = HybridWorkload(cfg, dev, rank, args.replicas, overlap=not args.no_lookup_overlap)
+    elif args.workload in wl.FILL_CONFIGS:
+        W = FillWorkload(args.workload, dev, rank, args.batch)
     else:
         pc = wl.PAGED_CONFIGS[args.workload]
         if args.batch:
@@ -599,9 +733,14 @@ def run_ours(args):
 
     attn_ms_mean = statistics.fmean(attn_ms)
     achieved = W.attn_bytes_per_launch() / (attn_ms_mean * 1e-3) / 1e9
-    peak, peak_src = peak_hbm()
-    kernel_src = os.path.join(ROOT, "offloaded_kv_decode_gb300", "csrc", "clo_attention.cu")
-    traffic = traffic_from_profiles(kernel_src, args.workload)
+    if hasattr(W, "roofline_peak"):
+        peak, peak_src, bound = W.roofline_peak()
+    else:
+        (peak, peak_src), bound = peak_hbm(), "hbm"
+    kernel = getattr(W, "kernel", "attn_split_kernel")
+    kernel_src = os.path.join(ROOT, "offloaded_kv_decode_gb300", "csrc",
+                              getattr(W, "kernel_src", "clo_attention.cu"))
+    traffic = traffic_from_profiles(kernel_src, kernel, args.workload)
 
     # End to end through the public API with host buffers.
     e2e = None
@@ -646,10 +785,10 @@ def run_ours(args):
         "dtype": "f16",
         "data": "synthetic (seeded; shapes of the pages' workloads)",
         "config": W.config(),
-        "hbm_frac_of_measured_peak": value / world / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "step_frac_of_peak": value / world / peak,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "attn_split_kernel", "peak_source": peak_src,
+                     "kernel": kernel, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": W.attn_bytes_per_launch(),
                      "launch_ms_mean": attn_ms_mean, "launch_samples": len(attn_ms)},
         "cpu_baseline": cpu,
@@ -711,7 +850,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(list(wl.CONFIGS) + list(wl.PAGED_CONFIGS)))
+                    choices=sorted(list(wl.CONFIGS) + list(wl.PAGED_CONFIGS) +
+                                   list(wl.FILL_CONFIGS)))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--max-rounds", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0,

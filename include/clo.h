@@ -121,12 +121,52 @@ clo_status clo_lookup_update(const clo_half* q, clo_half* labels,
                              int32_t* miss_list, int32_t* miss_count,
                              cudaStream_t stream);
 
-/* Optional tuning and instrumentation for the attention calls (may be NULL). */
+/* Optional tuning and instrumentation for the attention and fill calls (may
+ * be NULL).  Events recorded while `stream` is being captured into a CUDA
+ * graph become external event nodes, so they can time replays. */
 typedef struct clo_attn_opts {
-    int num_ctas;         /* CTAs of the main kernel; 0 = one per SM */
+    int num_ctas;         /* CTAs of the main kernel; 0 = the default (one full wave) */
     cudaEvent_t ev_begin; /* if non-NULL, recorded on `stream` right before the main kernel */
     cudaEvent_t ev_end;   /* if non-NULL, recorded right after the main kernel */
 } clo_attn_opts;
+
+/*
+ * clo_fill_cache_buffer -- miss-path fill of the Cache Buffer (CLO section 3
+ * Fig. 7: an update writes the new KV data straight to its final position,
+ * with no staging buffer and no second copy; section 2: only the KV heads
+ * that missed are transferred).  For every entry e = b*Hkv + g of
+ * miss_list[0 .. *miss_count) and every j < k:
+ *     cbK[e][slot[e][j]] = srcK[e][tok[e][j]]   (and the same for V)
+ * srcK, srcV: [B][Hkv][T][d] fp16, the full KV copy.  Either device memory or
+ *             pinned host memory mapped into the device's address space
+ *             (cudaHostAlloc, a pinned torch tensor): the kernel then reads
+ *             the rows in place over the host link (NVLink-C2C on GB300).
+ *             Other host memory is accepted only where the device can read
+ *             pageable memory; a source the device cannot read gives
+ *             CLO_ERR_INVALID_ARG and nothing is launched.
+ * tok:        [B][Hkv][k] int32 (device): token of the j-th row of each
+ *             head's new top-k set.
+ * slot:       [B][Hkv][k] int32 (device): its row in the Cache Buffer, i.e.
+ *             the index the hybrid attention will read it through; NULL
+ *             means slot = tok (token-addressed buffer, requires C >= T).
+ *             The slots of one head must be distinct.
+ * cbK, cbV:   [B][Hkv][C][d] fp16 (device), written in place; rows of heads
+ *             not on the list and rows not named by a slot are not touched.
+ * miss_list, miss_count: device arrays as written by clo_lookup_update (the
+ *             count is read on the device; the call does not synchronise).
+ * err_flag:   optional (device).  A list entry outside [0, B*Hkv), a token
+ *             outside [0, T) or a slot outside [0, C) sets CLO_FLAG_BAD_INDEX
+ *             and that row (or head) is skipped; a count outside [0, B*Hkv]
+ *             sets it and is clamped.
+ * opts:       optional (see clo_attn_opts).
+ * Requires d == 128; pointers to K/V 16-byte aligned.
+ */
+clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int T,
+                                 const int32_t* tok, const int32_t* slot, int k,
+                                 clo_half* cbK, clo_half* cbV, int C,
+                                 const int32_t* miss_list, const int32_t* miss_count,
+                                 int B, int Hkv, int d, int32_t* err_flag,
+                                 const clo_attn_opts* opts, cudaStream_t stream);
 
 /*
  * Workspace bytes clo_hybrid_decode_attn needs for these sizes when run with

@@ -54,6 +54,8 @@ _SIGS = {
     "clo_check_error_flag": ([ctypes.c_int32], _I),
     "clo_thresholds": ([_P, _I, _I, _F, _F, _P, _P], _I),
     "clo_lookup_update": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "clo_fill_cache_buffer": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P,
+                               _P], _I),
     "clo_hybrid_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_hybrid_decode_attn": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _F, _P, _P, _P, _SZ, _P, _P, _P], _I),
@@ -125,6 +127,19 @@ def _dev(t: Optional[torch.Tensor], name: str, dtype, ndim=None, optional=False)
     return t.data_ptr()
 
 
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype, ndim) -> int:
+    """A CUDA tensor, or a pinned host tensor the device reads in place."""
+    if t is not None and not t.is_cuda:
+        if not t.is_pinned():
+            raise CloError(f"{name} must be a CUDA tensor or pinned host memory",
+                           CLO_ERR_INVALID_ARG)
+        if t.dtype != dtype or not t.is_contiguous() or t.dim() != ndim:
+            raise CloError(f"{name} must be a contiguous {ndim}-d {dtype} tensor",
+                           CLO_ERR_INVALID_ARG)
+        return t.data_ptr()
+    return _dev(t, name, dtype, ndim)
+
+
 def _events(events) -> tuple:
     if events is None:
         return 0, 0
@@ -180,6 +195,41 @@ def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
         raise CloError("lookup buffer sizes do not match q / tau_kv", CLO_ERR_INVALID_ARG)
     _check(lib().clo_lookup_update(pq, pl, pw, pt, pm, B, Hq, Hkv, d, pf, psim, pml, pmc,
                                    _stream(stream)), "clo_lookup_update")
+
+
+# ---------------------------------------------------------------- miss-path fill
+
+def clo_fill_cache_buffer(srcK: torch.Tensor, srcV: torch.Tensor, tok: torch.Tensor,
+                          slot: Optional[torch.Tensor], cbK: torch.Tensor, cbV: torch.Tensor,
+                          miss_list: torch.Tensor, miss_count: torch.Tensor,
+                          err_flag: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                          events: Optional[Sequence] = None, stream=None):
+    """Copies the new top-k rows of every missed KV head from the full KV copy
+    (srcK/srcV [B][Hkv][T][d], CUDA or pinned host memory) into the Cache
+    Buffer (cbK/cbV [B][Hkv][C][d]) at slot[b][g][j] (tok itself when slot is
+    None); tok/slot [B][Hkv][k] int32, miss_list/miss_count as written by
+    clo_lookup_update."""
+    ps = _dev_or_pinned(srcK, "srcK", torch.float16, 4)
+    pv = _dev_or_pinned(srcV, "srcV", torch.float16, 4)
+    B, Hkv, T, d = srcK.shape
+    if srcV.shape != srcK.shape:
+        raise CloError("srcV must match srcK", CLO_ERR_INVALID_ARG)
+    pt = _dev(tok, "tok", torch.int32, 3)
+    k = tok.shape[2]
+    psl = _dev(slot, "slot", torch.int32, 3, optional=True)
+    pk = _dev(cbK, "cbK", torch.float16, 4)
+    pcv = _dev(cbV, "cbV", torch.float16, 4)
+    C = cbK.shape[2]
+    if cbV.shape != cbK.shape or cbK.shape[:2] != (B, Hkv) or cbK.shape[3] != d or \
+            tok.shape[:2] != (B, Hkv) or (slot is not None and slot.shape != tok.shape):
+        raise CloError("fill shapes do not match", CLO_ERR_INVALID_ARG)
+    pml = _dev(miss_list, "miss_list", torch.int32)
+    pmc = _dev(miss_count, "miss_count", torch.int32)
+    pe = _dev(err_flag, "err_flag", torch.int32, optional=True)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_fill_cache_buffer(ps, pv, T, pt, psl, k, pk, pcv, C, pml, pmc, B, Hkv, d,
+                                       pe, None if opts is None else ctypes.byref(opts),
+                                       _stream(stream)), "clo_fill_cache_buffer")
 
 
 # ---------------------------------------------------------------- attention

@@ -1018,31 +1018,11 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-static int device_sm_count() {
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
-
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Records a timing event on the stream.  Under stream capture the record is
 // made external so it becomes an event node of the graph (re-recorded on
 // every replay) rather than an internal ordering edge.
-static bool record_event(cudaEvent_t ev, cudaStream_t stream) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return false;
-    if (cs == cudaStreamCaptureStatusActive)
-        return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal) == cudaSuccess;
-    return cudaEventRecord(ev, stream) == cudaSuccess;
-}
-
 static size_t partial_bytes(long long slots, int G) {
     const size_t o = static_cast<size_t>(slots) * G * D * sizeof(float);
     const size_t l = static_cast<size_t>(slots) * G * sizeof(float);

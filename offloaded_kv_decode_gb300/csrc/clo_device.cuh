@@ -124,6 +124,29 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Records ev on stream; under stream capture as an external event node, so
+// the event still times graph replays.
+inline bool record_event(cudaEvent_t ev, cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return false;
+    if (cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal) == cudaSuccess;
+    return cudaEventRecord(ev, stream) == cudaSuccess;
+}
+
+// SM count of the current device, looked up once per device.
+inline int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 // Applies the launch attributes every libclo kernel shares, once per
 // (kernel, device): the maximum shared-memory carveout (so consecutive libclo
 // kernels never make the SMs switch their L1/shared split) and, if

@@ -1,0 +1,204 @@
+// clo_fill.cu -- miss-path fill of the Cache Buffer (CLO section 3, Fig. 7:
+// an update writes the new KV rows straight to their final position, with no
+// staging buffer; section 2: only the heads that missed are transferred), for
+// sm_103a.
+//
+// For every KV head on the miss list (as written by the lookup) the rows of
+// its new top-k token set are copied from the full KV copy into the Cache
+// Buffer rows the hybrid attention reads.  The full copy may sit in pinned
+// host memory: the kernel then reads it in place over NVLink-C2C, which takes
+// the place of CLO's GDRCopy transfer engine (the GPU pulls the rows itself,
+// so no CPU thread gathers or pushes them).
+//
+// Work is a flat line of rows (miss m, row j), m < *miss_count (read on the
+// device, so the launch does not wait for the lookup's result on the host).
+// A warp takes 16 rows at a time: lanes 0..15 load the rows' list entry,
+// token and slot in parallel, then each half-warp moves 8 rows of K and 8 of
+// V (256 bytes each, 16 bytes a lane), all loads before any store, so every
+// lane has 16 independent 16-byte loads in flight across the host link.
+#include "clo_device.cuh"
+
+namespace clo {
+
+constexpr int FILL_D = 128;  // head dimension (fp16 elements a row)
+constexpr int FILL_THREADS = 256;
+constexpr int FILL_WARPS = FILL_THREADS / 32;
+constexpr int FILL_ROWS = 16;  // rows a warp moves per step
+constexpr int FILL_CTAS_PER_SM = 2;
+
+struct FillParams {
+    const clo_half* srcK;
+    const clo_half* srcV;
+    const int32_t* tok;
+    const int32_t* slot;  // nullptr: slot = token
+    clo_half* cbK;
+    clo_half* cbV;
+    const int32_t* miss_list;
+    const int32_t* miss_count;
+    int32_t* err_flag;
+    int T, k, C, n_heads;  // n_heads = B * Hkv
+};
+
+// A 16-byte load that does not allocate in L1 (the source is read once).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_row(void* p, const uint4& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM) fill_kernel(const FillParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the miss list comes from the kernel before
+    int count = *p.miss_count;
+    if (count < 0 || count > p.n_heads) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report_error(p.err_flag, CLO_FLAG_BAD_INDEX);
+        count = count < 0 ? 0 : p.n_heads;
+    }
+    const long long rows = static_cast<long long>(count) * p.k;
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4, chunk = lane & 15;
+    const long long warp0 = static_cast<long long>(blockIdx.x) * FILL_WARPS + (threadIdx.x >> 5);
+    const long long nwarps = static_cast<long long>(gridDim.x) * FILL_WARPS;
+    bool bad = false;
+    for (long long base = warp0 * FILL_ROWS; base < rows; base += nwarps * FILL_ROWS) {
+        // Lane i < 16 resolves row base + i: its head entry, token and slot.
+        long long src_row = -1, dst_row = -1;
+        const long long i = base + chunk;
+        if (lane < FILL_ROWS && i < rows) {
+            const int m = static_cast<int>(i / p.k);
+            const int j = static_cast<int>(i - static_cast<long long>(m) * p.k);
+            const int e = __ldg(p.miss_list + m);
+            if (e >= 0 && e < p.n_heads) {
+                const long long sel = static_cast<long long>(e) * p.k + j;
+                const int t = __ldg(p.tok + sel);
+                const int r = p.slot != nullptr ? __ldg(p.slot + sel) : t;
+                if (t >= 0 && t < p.T && r >= 0 && r < p.C) {
+                    src_row = static_cast<long long>(e) * p.T + t;
+                    dst_row = static_cast<long long>(e) * p.C + r;
+                } else {
+                    bad = true;
+                }
+            } else {
+                bad = true;
+            }
+        }
+        // Half-warp h moves rows h, h + 2, ..., h + 14 of the 16.
+        uint4 vk[FILL_ROWS / 2], vv[FILL_ROWS / 2];
+        long long dst[FILL_ROWS / 2];
+#pragma unroll
+        for (int u = 0; u < FILL_ROWS / 2; ++u) {
+            const int r = 2 * u + half;
+            const long long s = __shfl_sync(FULL_MASK, src_row, r);
+            dst[u] = __shfl_sync(FULL_MASK, dst_row, r);
+            if (s >= 0) {
+                vk[u] = ld_stream(p.srcK + s * FILL_D + chunk * 8);
+                vv[u] = ld_stream(p.srcV + s * FILL_D + chunk * 8);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < FILL_ROWS / 2; ++u) {
+            if (dst[u] >= 0) {
+                st_row(p.cbK + dst[u] * FILL_D + chunk * 8, vk[u]);
+                st_row(p.cbV + dst[u] * FILL_D + chunk * 8, vv[u]);
+            }
+        }
+    }
+    if (bad) report_error(p.err_flag, CLO_FLAG_BAD_INDEX);
+}
+
+// Resolves the address the device reads a source buffer through.  Device and
+// managed memory are used as they are; pinned host memory through its mapped
+// device address; other host memory only where the device can read pageable
+// memory (address translation services).  Returns false if the device cannot
+// read it, so no kernel is launched on an unreachable pointer.
+static bool device_readable(const void*& p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    if (a.type == cudaMemoryTypeHost) {
+        if (a.devicePointer == nullptr) return false;
+        p = a.devicePointer;
+        return true;
+    }
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess)
+        return false;
+    return pageable != 0;
+}
+
+}  // namespace clo
+
+using namespace clo;
+
+extern "C" clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int T,
+                                            const int32_t* tok, const int32_t* slot, int k,
+                                            clo_half* cbK, clo_half* cbV, int C,
+                                            const int32_t* miss_list, const int32_t* miss_count,
+                                            int B, int Hkv, int d, int32_t* err_flag,
+                                            const clo_attn_opts* opts, cudaStream_t stream) {
+    if (B < 0 || Hkv <= 0 || T < 0 || k < 0 || C < 0) return CLO_ERR_INVALID_ARG;
+    if (d != FILL_D) return CLO_ERR_UNSUPPORTED;
+    if (miss_count == nullptr) return CLO_ERR_INVALID_ARG;
+    const long long n_heads = static_cast<long long>(B) * Hkv;
+    if (n_heads > (1ll << 30) || static_cast<long long>(T) * n_heads > (1ll << 40) ||
+        static_cast<long long>(C) * n_heads > (1ll << 40))
+        return CLO_ERR_UNSUPPORTED;
+    if (B == 0 || k == 0) return CLO_OK;  // nothing to move
+    if (srcK == nullptr || srcV == nullptr || tok == nullptr || cbK == nullptr ||
+        cbV == nullptr || miss_list == nullptr)
+        return CLO_ERR_INVALID_ARG;
+    if (slot == nullptr && C < T) return CLO_ERR_INVALID_ARG;  // token-addressed needs C >= T
+    const auto aligned = [](const void* q, size_t a) {
+        return (reinterpret_cast<uintptr_t>(q) % a) == 0;
+    };
+    if (!aligned(srcK, 16) || !aligned(srcV, 16) || !aligned(cbK, 16) || !aligned(cbV, 16) ||
+        !aligned(tok, 4) || !aligned(slot, 4) || !aligned(miss_list, 4) || !aligned(miss_count, 4))
+        return CLO_ERR_INVALID_ARG;
+
+    const void* rK = srcK;
+    const void* rV = srcV;
+    if (!device_readable(rK) || !device_readable(rV)) return CLO_ERR_INVALID_ARG;
+
+    FillParams p;
+    p.srcK = static_cast<const clo_half*>(rK);
+    p.srcV = static_cast<const clo_half*>(rV);
+    p.tok = tok;
+    p.slot = slot;
+    p.cbK = cbK;
+    p.cbV = cbV;
+    p.miss_list = miss_list;
+    p.miss_count = miss_count;
+    p.err_flag = err_flag;
+    p.T = T;
+    p.k = k;
+    p.C = C;
+    p.n_heads = static_cast<int>(n_heads);
+    // One wave, no more warps than 16-row steps of the largest possible list.
+    const int sms = device_sm_count();
+    if (sms <= 0) return CLO_ERR_CUDA;
+    const long long max_steps = (n_heads * k + FILL_ROWS - 1) / FILL_ROWS;
+    long long grid = (max_steps + FILL_WARPS - 1) / FILL_WARPS;
+    if (grid > static_cast<long long>(sms) * FILL_CTAS_PER_SM) grid = static_cast<long long>(sms) * FILL_CTAS_PER_SM;
+    if (opts != nullptr && opts->num_ctas > 0) grid = opts->num_ctas;
+    if (grid < 1) grid = 1;
+    if (opts != nullptr && opts->ev_begin != nullptr && !record_event(opts->ev_begin, stream))
+        return CLO_ERR_CUDA;
+    if (launch_pdl(fill_kernel, dim3(static_cast<unsigned>(grid)), dim3(FILL_THREADS), 0, stream, p) !=
+        cudaSuccess)
+        return CLO_ERR_CUDA;
+    if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
+        return CLO_ERR_CUDA;
+    return CLO_OK;
+}

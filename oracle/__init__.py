@@ -191,13 +191,19 @@ class Oracle:
             raise ValueError(f"oracle_paged_attn rc={rc}")
         return out, lse
 
-    def fill_cache_buffer(self, srcK, srcV, tok, slot, cbK, cbV, miss_list):
+    def fill_cache_buffer(self, srcK, srcV, tok, slot, cbK, cbV, miss_list, inplace=False):
         """Miss-path fill.  srcK/srcV [B][Hkv][T][d], tok/slot [B][Hkv][k]
-        (slot None: token-addressed), cbK/cbV [B][Hkv][C][d] (not modified;
-        filled copies are returned), miss_list [n] -> (cbK, cbV, rc) with rc
-        0 or BAD_INDEX."""
+        (slot None: token-addressed), cbK/cbV [B][Hkv][C][d] (copied unless
+        inplace, in which case they must be contiguous and are written),
+        miss_list [n] -> (cbK, cbV, rc) with rc 0 or BAD_INDEX."""
         srcK, srcV = self._u16(srcK), self._u16(srcV)
-        outK, outV = self._u16(cbK).copy(), self._u16(cbV).copy()
+        if inplace:
+            outK, outV = self._u16(cbK), self._u16(cbV)
+            if outK.ctypes.data != np.asarray(cbK).ctypes.data or \
+                    outV.ctypes.data != np.asarray(cbV).ctypes.data:
+                raise ValueError("inplace fill needs contiguous fp16 Cache Buffer arrays")
+        else:
+            outK, outV = self._u16(cbK).copy(), self._u16(cbV).copy()
         tok = self._i32(tok)
         sl = None if slot is None else self._i32(slot)
         ml = self._i32(miss_list).ravel()

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -125,3 +125,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(clo, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(clo.CloError):
         clo.lib()
+
+
+def _fill(L, srcK=FAKE, T=64, tok=FAKE, slot=FAKE, k=8, C=64, ml=FAKE, mc=FAKE, B=1, Hkv=8, d=128):
+    return L.clo_fill_cache_buffer(srcK, FAKE, T, tok, slot, k, FAKE, FAKE, C, ml, mc, B, Hkv, d,
+                                   None, None, None)
+
+
+def test_fill_rejects(L):
+    assert _fill(L, srcK=None) == clo.CLO_ERR_INVALID_ARG
+    assert _fill(L, tok=None) == clo.CLO_ERR_INVALID_ARG
+    assert _fill(L, ml=None) == clo.CLO_ERR_INVALID_ARG
+    assert _fill(L, mc=None) == clo.CLO_ERR_INVALID_ARG
+    assert _fill(L, slot=None, C=32) == clo.CLO_ERR_INVALID_ARG  # token rows need C >= T
+    assert _fill(L, srcK=FAKE + 2) == clo.CLO_ERR_INVALID_ARG    # misaligned fp16 rows
+    assert _fill(L, B=-1) == clo.CLO_ERR_INVALID_ARG
+    assert _fill(L, d=64) == clo.CLO_ERR_UNSUPPORTED
+    assert _fill(L, k=0) == clo.CLO_OK                           # nothing to move: no launch
+    assert _fill(L, B=0) == clo.CLO_OK

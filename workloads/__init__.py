@@ -118,6 +118,15 @@ PAGED_CONFIGS = {
 }
 
 
+# Miss-path fill: the Cache Buffer rows of every non-persistent KV head of the
+# Llama3-8B-shaped batch-8 layer refilled from the full KV copy, which sits in
+# pinned host memory (read over the host link) or in HBM.
+FILL_CONFIGS = {
+    "fill_c2c_llama3_8b_b8_32k": ("llama3_8b_layer_b8_32k", "host"),
+    "fill_hbm_llama3_8b_b8_32k": ("llama3_8b_layer_b8_32k", "device"),
+}
+
+
 def small_hybrid(name="small", **kw) -> HybridConfig:
     """A reduced workload for quick parity runs (any field overridable)."""
     base = dict(B=2, L=1, Hq=32, Hkv=8, T=1000, Np=2, qmode="mix",
@@ -227,6 +236,32 @@ def persistent_cache(cfg: HybridConfig, layer: int, device="cpu"):
     pK = torch.randn(shape, generator=g, device=device, dtype=torch.float16)
     pV = torch.randn(shape, generator=g, device=device, dtype=torch.float16)
     return pK, pV
+
+
+def full_kv(cfg: HybridConfig, layer: int, device="cpu"):
+    """(srcK, srcV): the full KV copy of every head, fp16 [B][Hkv][T][d] ~ N(0,1)
+    (what the miss-path fill reads from)."""
+    g = _torch_gen(device, _seed(cfg.seed, layer, 6))
+    shape = (cfg.B, cfg.Hkv, cfg.T, cfg.d)
+    srcK = torch.randn(shape, generator=g, device=device, dtype=torch.float16)
+    srcV = torch.randn(shape, generator=g, device=device, dtype=torch.float16)
+    return srcK, srcV
+
+
+def fill_selection(cfg: HybridConfig, layer: int, device="cpu"):
+    """(tok, slot) int32 [B][Hkv][k]: each head's new top-k token set (k
+    distinct tokens of [0, T), unsorted) and the Cache Buffer row of each (the
+    token itself with token addressing, a permutation of [0, k) with compact
+    addressing)."""
+    g = _torch_gen(device, _seed(cfg.seed, layer, 7))
+    keys = torch.rand((cfg.B * cfg.Hkv, cfg.T), generator=g, device=device)
+    tok = keys.argsort(dim=1)[:, : cfg.k].to(torch.int32).reshape(cfg.B, cfg.Hkv, cfg.k)
+    if cfg.addressing == "token":
+        slot = tok.clone()
+    else:
+        keys = torch.rand((cfg.B * cfg.Hkv, cfg.k), generator=g, device=device)
+        slot = keys.argsort(dim=1).to(torch.int32).reshape(cfg.B, cfg.Hkv, cfg.k)
+    return tok.contiguous(), slot.contiguous()
 
 
 def paged_context_lengths(cfg: PagedConfig) -> np.ndarray:
