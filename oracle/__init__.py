@@ -72,6 +72,8 @@ class Oracle:
         lib.oracle_fill_cache_buffer.argtypes = [_P, _P, _I, _P, _P, _I, _P, _P, _I,
                                                  _P, _I, _I, _I, _I]
         lib.oracle_fill_cache_buffer.restype = _I
+        lib.oracle_plan_persistent.argtypes = [_P, _P, _I, _I, _D, _D, _D, _D, _P, _P, _P, _P]
+        lib.oracle_plan_persistent.restype = _I
         self.lib = lib
 
     # -- helpers ----------------------------------------------------------
@@ -217,6 +219,25 @@ class Oracle:
         if rc not in (OK, BAD_INDEX):
             raise ValueError(f"oracle_fill_cache_buffer rc={rc}")
         return outK, outV, rc
+
+    def plan_persistent(self, tau, s_hat, eps: float, t_comp: float, b_link: float,
+                        mem_head: float):
+        """Eqs. 11-13.  tau, s_hat [L][Hkv] -> dict(D [L][Hkv] f64, n_p int,
+        n_persist [L] int32, persist_ids [L][Hkv] int32, -1 padded)."""
+        tau, sh = self._f64(tau), self._f64(s_hat)
+        if tau.ndim != 2 or sh.shape != tau.shape:
+            raise ValueError("tau and s_hat must be [L][Hkv]")
+        L, Hkv = tau.shape
+        D = np.zeros((L, Hkv), dtype=np.float64)
+        n_p = np.zeros(1, dtype=np.int32)
+        n_persist = np.zeros(max(L, 1), dtype=np.int32)
+        ids = np.zeros((max(L, 1), Hkv), dtype=np.int32)
+        rc = self.lib.oracle_plan_persistent(_ptr(tau), _ptr(sh), L, Hkv, float(eps),
+                                             float(t_comp), float(b_link), float(mem_head),
+                                             _ptr(D), _ptr(n_p), _ptr(n_persist), _ptr(ids))
+        if rc != OK:
+            raise ValueError(f"oracle_plan_persistent rc={rc}")
+        return dict(D=D, n_p=int(n_p[0]), n_persist=n_persist[:L].copy(), persist_ids=ids[:L].copy())
 
 
 _default = None

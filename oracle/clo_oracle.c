@@ -30,6 +30,13 @@
  *                         for Online LLM Inference", method details, system
  *                         implementation and CPU kernel (vLLM-like paged KV
  *                         cache, one decode query per request); same attention.
+ *   oracle_plan_persistent  CLO page, section 3.3 and section 2 (selective
+ *                         residency): reuse difficulty D_i = tau_i - (s^_i - eps)
+ *                         (Eq. 11); the heads one layer's compute time can
+ *                         prefetch, N_p = floor(T_comp * B_link / mem_head)
+ *                         (Eq. 12); the heads of layer l kept resident,
+ *                         N_persist^l = max(N_hard^l - N_p, 0) with N_hard^l the
+ *                         heads of the layer with D_i > 0 (Eq. 13).
  *   oracle_fill_cache_buffer  CLO page, section 3, Fig. 7 (an update writes
  *                         the new KV data straight to its final position, no
  *                         staging buffer) and section 2 (only missed heads
@@ -50,6 +57,12 @@
  *   - The final position of a filled row is the Cache Buffer row that the
  *     attention's index names for it; with token-addressed buffers that row
  *     is the token itself.
+ *   - Eq. 12 as printed divides T_comp by B_link * mem_head, which is not
+ *     dimensionless; the count of heads one layer can prefetch is taken as
+ *     T_comp * B_link / mem_head, rounded down.
+ *   - Of the hard heads (D_i > 0, strictly) of a layer, the N_persist^l with
+ *     the largest D_i are kept resident (the rest are prefetched); equal D_i
+ *     are taken in increasing head order.
  */
 #include <math.h>
 #include <stdint.h>
@@ -342,4 +355,50 @@ int oracle_fill_cache_buffer(const uint16_t* srcK, const uint16_t* srcV, int T,
         }
     }
     return rc;
+}
+
+/* Offline persistent-head plan, Eqs. 11-13.
+ *   tau, s_hat  [L][Hkv]  per-KV-head threshold and profiled mean cosine
+ *   eps         tolerance margin of Eq. 11
+ *   t_comp      one layer's compute time (s); b_link the host link's bandwidth
+ *               (bytes/s); mem_head the top-k KV bytes of one head
+ * Outputs: D [L][Hkv] (Eq. 11), *n_p (Eq. 12), n_persist [L] (Eq. 13) and
+ * persist_ids [L][Hkv]: row l lists its n_persist[l] resident heads, largest
+ * D first, then -1. */
+int oracle_plan_persistent(const double* tau, const double* s_hat, int L, int Hkv,
+                           double eps, double t_comp, double b_link, double mem_head,
+                           double* D, int* n_p, int* n_persist, int* persist_ids) {
+    if (L < 0 || Hkv <= 0 || !(mem_head > 0) || !(t_comp >= 0) || !(b_link >= 0))
+        return ORACLE_BAD_ARG;
+    double cap = floor(t_comp * b_link / mem_head); /* Eq. 12 */
+    if (cap > 2147483647.0) cap = 2147483647.0;
+    *n_p = (int)cap;
+    for (int l = 0; l < L; ++l) {
+        int hard = 0;
+        for (int i = 0; i < Hkv; ++i) {
+            size_t at = (size_t)l * Hkv + i;
+            D[at] = tau[at] - (s_hat[at] - eps); /* Eq. 11 */
+            if (D[at] > 0) ++hard;
+            persist_ids[at] = -1;
+        }
+        int keep = hard - *n_p; /* Eq. 13 */
+        if (keep < 0) keep = 0;
+        n_persist[l] = keep;
+        /* Pick the keep hardest heads one at a time: the largest D not yet
+         * taken, the lower head index on a tie. */
+        for (int j = 0; j < keep; ++j) {
+            int best = -1;
+            for (int i = 0; i < Hkv; ++i) {
+                size_t at = (size_t)l * Hkv + i;
+                if (!(D[at] > 0)) continue;
+                int taken = 0;
+                for (int u = 0; u < j; ++u)
+                    if (persist_ids[(size_t)l * Hkv + u] == i) taken = 1;
+                if (taken) continue;
+                if (best < 0 || D[at] > D[(size_t)l * Hkv + best]) best = i;
+            }
+            persist_ids[(size_t)l * Hkv + j] = best;
+        }
+    }
+    return ORACLE_OK;
 }

@@ -543,6 +543,82 @@ def pin_fill_list_order(orc):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+# -- offline persistent-head plan (CLO page, section 3.3, Eqs. 11-13) ---------
+
+_PLAN_TAU = [[0.8, 0.5, -1.0, 0.7], [0.6, 0.6, 0.2, -0.5]]
+_PLAN_SHAT = [[0.75, 0.9, 0.2, 0.5], [0.4, 0.45, 0.9, 0.1]]
+
+
+def pin_plan_worked_example(orc):
+    """Eqs. 11-13 on numbers worked out by hand.  D = tau - (s^ - 0.1):
+    layer 0: 0.15, -0.3, -1.1, 0.3 (hard: heads 3, 0); layer 1: 0.3, 0.25,
+    -0.6, -0.5 (hard: heads 0, 1).  mem_head = 10 MB over 10 GB/s: one head
+    per ms of compute."""
+    want_D = [[0.15, -0.3, -1.1, 0.3], [0.3, 0.25, -0.6, -0.5]]
+    for t_comp, n_p, n_persist, ids in (
+            (0.5e-3, 0, [2, 2], [[3, 0, -1, -1], [0, 1, -1, -1]]),
+            (1.5e-3, 1, [1, 1], [[3, -1, -1, -1], [0, -1, -1, -1]]),
+            (2.5e-3, 2, [0, 0], [[-1] * 4, [-1] * 4]),
+            (40e-3, 40, [0, 0], [[-1] * 4, [-1] * 4])):
+        r = orc.plan_persistent(_PLAN_TAU, _PLAN_SHAT, 0.1, t_comp, 10e9, 10e6)
+        assert np.allclose(r["D"], want_D, atol=1e-12, rtol=0), r["D"]
+        assert r["n_p"] == n_p, (t_comp, r["n_p"])
+        assert r["n_persist"].tolist() == n_persist, (t_comp, r["n_persist"])
+        assert r["persist_ids"].tolist() == ids, (t_comp, r["persist_ids"])
+
+
+def pin_plan_zero_difficulty_is_not_hard(orc):
+    """D = 0 exactly (0.5 - (0.75 - 0.25)) is not hard: Eq. 11 needs D > 0."""
+    r = orc.plan_persistent([[0.5, 0.5]], [[0.75, 0.5]], 0.25, 0.0, 1e9, 1e6)
+    assert r["D"].tolist() == [[0.0, 0.25]]
+    assert r["n_p"] == 0 and r["n_persist"].tolist() == [1]
+    assert r["persist_ids"].tolist() == [[1, -1]]
+
+
+def pin_plan_tie_goes_to_lower_head(orc):
+    """Heads 1 and 2 are equally hard (D = 0.2) and harder than head 0
+    (D = 0.1); with one head to keep, head 1 is kept, with two, heads 1, 2."""
+    tau, sh = [[0.5, 0.6, 0.6]], [[0.4, 0.4, 0.4]]   # D = tau - s^ (eps = 0)
+    r = orc.plan_persistent(tau, sh, 0.0, 2.5e-3, 1e9, 1e6)    # N_p = 2 of 3 hard
+    assert r["n_p"] == 2 and r["n_persist"].tolist() == [1]
+    assert r["persist_ids"].tolist() == [[1, -1, -1]]
+    r = orc.plan_persistent(tau, sh, 0.0, 1.5e-3, 1e9, 1e6)    # N_p = 1
+    assert r["persist_ids"].tolist() == [[1, 2, -1]]
+
+
+def pin_plan_invariants(orc):
+    """Random plans: N_p is dimensionless (scaling time and head bytes
+    together leaves it alone), Eq. 13 is never negative, more bandwidth never
+    keeps more heads resident, the resident heads are the hardest ones, and
+    ties go to the lower head index."""
+    rng = _rng(61)
+    L, Hkv = 6, 8
+    tau = rng.uniform(-1, 0.8, (L, Hkv))
+    sh = rng.uniform(0.2, 1.0, (L, Hkv))
+    tau[2, 5] = tau[2, 1]
+    sh[2, 5] = sh[2, 1]          # equal difficulty in layer 2
+    last = None
+    for bw in (0.0, 1e9, 3e9, 6e9, 2e10):
+        r = orc.plan_persistent(tau, sh, 0.05, 2e-3, bw, 2e6)
+        r2 = orc.plan_persistent(tau, sh, 0.05, 4e-3, bw, 4e6)
+        assert r2["n_p"] == r["n_p"]
+        hard = (r["D"] > 0).sum(axis=1)
+        assert np.array_equal(r["n_persist"], np.maximum(hard - r["n_p"], 0))
+        assert (r["n_persist"] >= 0).all()
+        if last is not None:
+            assert (r["n_persist"] <= last).all()
+        last = r["n_persist"]
+        for l in range(L):
+            kept = [i for i in r["persist_ids"][l] if i >= 0]
+            assert len(kept) == r["n_persist"][l] and len(set(kept)) == len(kept)
+            rest = [i for i in range(Hkv) if r["D"][l, i] > 0 and i not in kept]
+            if kept and rest:
+                assert min(r["D"][l, kept]) >= max(r["D"][l, rest])
+            assert list(r["D"][l, kept]) == sorted(r["D"][l, kept], reverse=True)
+            if l == 2 and 5 in kept:   # the tie: head 1 goes first
+                assert 1 in kept and kept.index(1) < kept.index(5)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

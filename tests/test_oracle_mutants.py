@@ -49,6 +49,16 @@ MUTANTS = [
     ("fill miss list ignored", "int e = miss_list[m];", "int e = m;"),
     ("fill source row by position", "size_t from = ((size_t)e * T + t) * d;",
      "size_t from = ((size_t)e * T + j) * d;"),
+    ("Eq. 11 margin sign", "D[at] = tau[at] - (s_hat[at] - eps);",
+     "D[at] = tau[at] - (s_hat[at] + eps);"),
+    ("Eq. 12 as printed", "double cap = floor(t_comp * b_link / mem_head);",
+     "double cap = floor(t_comp / (b_link * mem_head));"),
+    ("Eq. 13 clamp dropped", "if (keep < 0) keep = 0;", ""),
+    ("hard at zero difficulty", "if (D[at] > 0) ++hard;", "if (D[at] >= 0) ++hard;"),
+    ("easiest heads kept", "if (best < 0 || D[at] > D[(size_t)l * Hkv + best]) best = i;",
+     "if (best < 0 || D[at] < D[(size_t)l * Hkv + best]) best = i;"),
+    ("tie goes to the higher head", "if (best < 0 || D[at] > D[(size_t)l * Hkv + best]) best = i;",
+     "if (best < 0 || D[at] >= D[(size_t)l * Hkv + best]) best = i;"),
     ("fill last row dropped", "for (int j = 0; j < k; ++j) {\n            size_t sel",
      "for (int j = 0; j < k - 1; ++j) {\n            size_t sel"),
 ]
