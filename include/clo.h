@@ -121,6 +121,32 @@ clo_status clo_lookup_update(const clo_half* q, clo_half* labels,
                              int32_t* miss_list, int32_t* miss_count,
                              cudaStream_t stream);
 
+/*
+ * clo_plan_persistent -- offline persistent-head plan (CLO section 3.3 and
+ * section 2, selective residency; Eqs. 11-13).  Host function, no GPU work.
+ *     D_i         = tau_i - (s^_i - eps)                          Eq. 11
+ *     N_p         = floor(t_comp * link_bytes_per_s / head_bytes) Eq. 12
+ *     N_persist^l = max(#{i in layer l : D_i > 0} - N_p, 0)       Eq. 13
+ * (Eq. 12 as printed divides T_comp by B_link * mem_head, which is not
+ * dimensionless; the number of heads whose top-k rows one layer's compute
+ * time can bring over the link is taken.)  Layer l keeps its N_persist^l
+ * hardest heads resident (largest D first, ties to the lower head index):
+ * these are its persist_ids for clo_hybrid_decode_attn and its persistent
+ * mask for clo_lookup_update.
+ * tau, s_hat:  [L][Hkv] host fp32: thresholds (e.g. clo_thresholds) and the
+ *              offline-profiled mean query cosine of each KV head.
+ * eps:         tolerance margin (the page uses 0.1 for Llama3, 0.05 for Qwen2.5).
+ * t_comp_s:    one layer's compute time (s); link_bytes_per_s: host-link
+ *              bandwidth; head_bytes: top-k K+V bytes of one head (> 0).
+ * D:           [L][Hkv] host fp64 output (computed in fp64 from the inputs).
+ * n_p:         [1] output.  n_persist: [L] output.
+ * persist_ids: [L][Hkv] output; row l holds its n_persist[l] heads, then -1.
+ */
+clo_status clo_plan_persistent(const float* tau, const float* s_hat, int L, int Hkv,
+                               float eps, double t_comp_s, double link_bytes_per_s,
+                               double head_bytes, double* D, int32_t* n_p,
+                               int32_t* n_persist, int32_t* persist_ids);
+
 /* Optional tuning and instrumentation for the attention and fill calls (may
  * be NULL).  Events recorded while `stream` is being captured into a CUDA
  * graph become external event nodes, so they can time replays. */

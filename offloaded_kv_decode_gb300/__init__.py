@@ -56,6 +56,8 @@ _SIGS = {
     "clo_lookup_update": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "clo_fill_cache_buffer": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P,
                                _P], _I),
+    "clo_plan_persistent": ([_P, _P, _I, _I, _F, ctypes.c_double, ctypes.c_double,
+                             ctypes.c_double, _P, _P, _P, _P], _I),
     "clo_hybrid_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_hybrid_decode_attn": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _F, _P, _P, _P, _SZ, _P, _P, _P], _I),
@@ -195,6 +197,31 @@ def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
         raise CloError("lookup buffer sizes do not match q / tau_kv", CLO_ERR_INVALID_ARG)
     _check(lib().clo_lookup_update(pq, pl, pw, pt, pm, B, Hq, Hkv, d, pf, psim, pml, pmc,
                                    _stream(stream)), "clo_lookup_update")
+
+
+# ---------------------------------------------------------------- offline plan
+
+def clo_plan_persistent(tau, s_hat, eps: float, t_comp_s: float, link_bytes_per_s: float,
+                        head_bytes: float) -> dict:
+    """Eqs. 11-13 on the host: tau, s_hat [L][Hkv] (array-likes, fp32) ->
+    dict(D [L][Hkv] fp64, n_p, n_persist [L] int32, persist_ids [L][Hkv] int32,
+    -1 padded)."""
+    import numpy as np
+
+    t = np.ascontiguousarray(np.asarray(tau, dtype=np.float32))
+    s = np.ascontiguousarray(np.asarray(s_hat, dtype=np.float32))
+    if t.ndim != 2 or s.shape != t.shape:
+        raise CloError("tau and s_hat must be [L][Hkv]", CLO_ERR_INVALID_ARG)
+    L, Hkv = t.shape
+    D = np.zeros((L, Hkv), dtype=np.float64)
+    n_p = np.zeros(1, dtype=np.int32)
+    n_persist = np.zeros(max(L, 1), dtype=np.int32)
+    ids = np.zeros((max(L, 1), Hkv), dtype=np.int32)
+    _check(lib().clo_plan_persistent(t.ctypes.data, s.ctypes.data, L, Hkv, float(eps),
+                                     float(t_comp_s), float(link_bytes_per_s), float(head_bytes),
+                                     D.ctypes.data, n_p.ctypes.data, n_persist.ctypes.data,
+                                     ids.ctypes.data), "clo_plan_persistent")
+    return dict(D=D, n_p=int(n_p[0]), n_persist=n_persist[:L].copy(), persist_ids=ids[:L].copy())
 
 
 # ---------------------------------------------------------------- miss-path fill
