@@ -85,13 +85,13 @@ def paged_bytes(pc, ctx: np.ndarray) -> int:
 class HybridWorkload:
     kind = "hybrid"
 
-    def __init__(self, cfg, dev, rank: int, replicas: int = 0, overlap: bool = True):
+    def __init__(self, cfg, dev, rank: int, replicas: int = 0, schedule: str = "fused"):
         import torch
         import offloaded_kv_decode_gb300 as clo
 
         self.clo, self.torch = clo, torch
         self.cfg = cfg
-        self.overlap = overlap
+        self.schedule = schedule
         self.side = torch.cuda.Stream(dev)
         self.L = cfg.L
         per_layer = hybrid_attn_bytes(cfg)
@@ -143,6 +143,8 @@ class HybridWorkload:
         return hybrid_attn_bytes(self.cfg)
 
     def launches_per_step(self) -> int:
+        if self.schedule == "fused":  # main kernel + merge launch carrying the lookup
+            return 1 + self.L * 2
         return 1 + self.L * (1 + self.attn_kernels)
 
     def _lookup(self, step: int, l: int):
@@ -153,6 +155,16 @@ class HybridWorkload:
         self.clo.clo_lookup_update(it["q"], it["labels"], it["w"], tau, it["pmask"], it["flag"],
                                    it["sim"], it["miss"], it["nmiss"])
 
+    def _attention_lookup(self, step: int, l: int, events=None):
+        it = self.instance(step, l)
+        nx = self.instance(step, l + 1)
+        j = (step * self.L + l + 1) % self.n_inst
+        tau = self.tau[j * self.cfg.Hkv:(j + 1) * self.cfg.Hkv]
+        self.clo.clo_hybrid_decode_attn_lookup(
+            it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"], it["pV"], it["pid"], it["out"],
+            self.ws, nx["q"], nx["labels"], nx["w"], tau, nx["pmask"], nx["flag"], nx["sim"],
+            nx["miss"], nx["nmiss"], err_flag=self.err, events=events)
+
     def _attention(self, step: int, l: int, events=None):
         it = self.instance(step, l)
         self.clo.clo_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"],
@@ -160,16 +172,25 @@ class HybridWorkload:
                                         err_flag=self.err, events=events)
 
     def launch(self, step: int, attn_events=None):
-        """One decode step.  With overlap (the default) the lookup runs one
+        """One decode step.  With the "fused" schedule (the default) every
+        layer is one clo_hybrid_decode_attn_lookup call: the attention of
+        layer l with the lookup of layer l+1 carried in the same launch
+        sequence (the step's last call looks up the next step's layer 0, so
+        each step still runs exactly L lookups and L attentions).  With the
+        "stream" schedule the lookup runs one
         layer ahead on a second stream, as in CLO's decode flow: the lookup of
         layer l+1 starts when layer l starts (after attention l-1) and runs
         beside attention l, and the step's last lookup is the next step's
         layer 0 (replays of the step graph are ordered on the stream, so
-        attention 0 of a step always follows its lookup).  Each step still
-        runs exactly L lookups and L attentions.  Without overlap every layer
-        runs lookup then attention on one stream."""
+        attention 0 of a step always follows its lookup).  With the "serial"
+        schedule every layer runs lookup then attention on one stream."""
         clo, cfg, torch = self.clo, self.cfg, self.torch
-        if not self.overlap:
+        if self.schedule == "fused":
+            clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+            for l in range(self.L):
+                self._attention_lookup(step, l, None if attn_events is None else attn_events[l])
+            return
+        if self.schedule == "serial":
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
             for l in range(self.L):
                 self._lookup(step, l)
@@ -213,6 +234,21 @@ class HybridWorkload:
     def e2e_step(self, step: int):
         clo, cfg = self.clo, self.cfg
         clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+        if self.schedule == "fused":
+            # Per layer: the next layer's queries in, one fused call, this
+            # layer's output and the next layer's lookup results out.
+            for l in range(self.L):
+                jn = (step * self.L + l + 1) % self.n_inst
+                nx = self.inst[jn]
+                nx["q"].copy_(self.h_q[jn], non_blocking=True)
+                self._attention_lookup(step, l)
+                j = (step * self.L + l) % self.n_inst
+                self.h_out[j].copy_(self.inst[j]["out"], non_blocking=True)
+                self.h_flag[jn].copy_(nx["flag"], non_blocking=True)
+                self.h_sim[jn].copy_(nx["sim"], non_blocking=True)
+                self.h_miss[jn].copy_(nx["miss"], non_blocking=True)
+                self.h_nmiss[jn].copy_(nx["nmiss"], non_blocking=True)
+            return
         for l in range(self.L):
             j = (step * self.L + l) % self.n_inst
             it = self.inst[j]
@@ -233,8 +269,10 @@ class HybridWorkload:
         return {"workload": c.name, "batch": c.B, "layers": c.L, "q_heads": c.Hq,
                 "kv_heads": c.Hkv, "head_dim": c.d, "context": c.T, "top_k": c.k,
                 "persistent_heads": c.Np, "cache_buffer": c.addressing,
-                "lookup_schedule": ("one layer ahead on a second stream" if self.overlap
-                                    else "before each layer's attention, same stream"),
+                "lookup_schedule": {
+                    "fused": "next layer's lookup carried in each attention launch",
+                    "stream": "one layer ahead on a second stream",
+                    "serial": "before each layer's attention, same stream"}[self.schedule],
                 "physical_buffer_sets": self.n_inst,
                 "l2": f"inputs larger than L2: a buffer is re-read after "
                       f"{self.reuse_distance() / 2**30:.2f} GiB of other reads"}
@@ -641,7 +679,7 @@ def run_ours(args):
         cfg = wl.CONFIGS[args.workload]
         if args.batch:
             cfg = dataclasses.replace(cfg, B=args.batch)
-        W = HybridWorkload(cfg, dev, rank, args.replicas, overlap=not args.no_lookup_overlap)
+        W = HybridWorkload(cfg, dev, rank, args.replicas, schedule=args.lookup_schedule)
     elif args.workload in wl.FILL_CONFIGS:
         W = FillWorkload(args.workload, dev, rank, args.batch)
     else:
@@ -858,8 +896,10 @@ def main(argv=None):
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-lookup-overlap", action="store_true",
-                    help="run lookup and attention of each layer back to back on one stream")
+    ap.add_argument("--lookup-schedule", choices=["fused", "stream", "serial"], default="fused",
+                    help="fused: the next layer's lookup rides in each attention launch; "
+                         "stream: it runs one layer ahead on a second stream; serial: lookup "
+                         "then attention for every layer on one stream")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--replicas", type=int, default=0,

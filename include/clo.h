@@ -196,7 +196,7 @@ clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int
 
 /*
  * Workspace bytes clo_hybrid_decode_attn needs for these sizes when run with
- * num_ctas CTAs (0 = one per SM of the current device).  Returns 0 for
+ * num_ctas CTAs (0 = the default grid on the current device).  Returns 0 for
  * invalid sizes.  The workspace holds split-KV partial results; it needs no
  * initialisation and may be reused by later calls on the same stream.
  */
@@ -234,6 +234,28 @@ clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
                                   size_t ws_bytes, int32_t* err_flag,
                                   const clo_attn_opts* opts,
                                   cudaStream_t stream);
+
+/*
+ * clo_hybrid_decode_attn_lookup -- clo_hybrid_decode_attn for layer l and
+ * clo_lookup_update for the next layer in one launch sequence (CLO section 3
+ * Fig. 9: the next layer's lookup runs while the current layer computes; the
+ * separate lookup launch of each layer is saved, CLO section 5's concern with
+ * launch overhead).  The results are those of the two calls made separately
+ * (the lookup reads nothing the attention writes).  The lookup is carried by
+ * the attention's merge launch as one extra 8-CTA cluster and starts while the
+ * main attention kernel drains.
+ * Arguments up to err_flag: as clo_hybrid_decode_attn.  q_next .. miss_count_next:
+ * as clo_lookup_update for the next layer (same B, Hq, Hkv, d).  opts: as for
+ * clo_hybrid_decode_attn.
+ */
+clo_status clo_hybrid_decode_attn_lookup(
+    const clo_half* q, const clo_half* cbK, const clo_half* cbV, const int32_t* idx, int k, int C,
+    const clo_half* pK, const clo_half* pV, const int32_t* persist_ids, int Np, int T, int B,
+    int Hq, int Hkv, int d, float scale, clo_half* out, float* lse, void* workspace,
+    size_t ws_bytes, int32_t* err_flag, const clo_half* q_next, clo_half* labels_next,
+    const float* w_q_next, const float* tau_next, const uint8_t* persist_mask_next,
+    uint8_t* flag_next, float* sim_next, int32_t* miss_list_next, int32_t* miss_count_next,
+    const clo_attn_opts* opts, cudaStream_t stream);
 
 /*
  * clo_hybrid_decode_attn_noalloc -- clo_hybrid_decode_attn for callers that

@@ -64,6 +64,9 @@ _SIGS = {
     "clo_hybrid_decode_attn_noalloc": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I,
                                         _I, _F, _P, _P, _P, _P, _P], _I),
     "clo_hybrid_noalloc_max_scratch": ([], _SZ),
+    "clo_hybrid_decode_attn_lookup": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                       _F, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, _P], _I),
     "clo_paged_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_paged_decode_attn": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                _P, _SZ, _P, _P, _P], _I),
@@ -173,11 +176,7 @@ def clo_thresholds(s: torch.Tensor, tau: torch.Tensor, group: int = 1, eta: floa
 
 # ---------------------------------------------------------------- lookup
 
-def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
-                      tau_kv: torch.Tensor, persist_mask: Optional[torch.Tensor],
-                      flag: torch.Tensor, sim: torch.Tensor, miss_list: torch.Tensor,
-                      miss_count: torch.Tensor, stream=None):
-    """Fused head-wise cache lookup + Eq. 10 + label update (labels updated in place)."""
+def _lookup_args(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count):
     pq = _dev(q, "q", torch.float16, 3)
     pl = _dev(labels, "labels", torch.float16, 3)
     if labels.shape != q.shape:
@@ -195,8 +194,16 @@ def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
             miss_list.numel() < B * Hkv or miss_count.numel() < 1 or \
             (persist_mask is not None and persist_mask.numel() != Hkv):
         raise CloError("lookup buffer sizes do not match q / tau_kv", CLO_ERR_INVALID_ARG)
-    _check(lib().clo_lookup_update(pq, pl, pw, pt, pm, B, Hq, Hkv, d, pf, psim, pml, pmc,
-                                   _stream(stream)), "clo_lookup_update")
+    return (pq, pl, pw, pt, pm, B, Hq, Hkv, d, pf, psim, pml, pmc)
+
+
+def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
+                      tau_kv: torch.Tensor, persist_mask: Optional[torch.Tensor],
+                      flag: torch.Tensor, sim: torch.Tensor, miss_list: torch.Tensor,
+                      miss_count: torch.Tensor, stream=None):
+    """Fused head-wise cache lookup + Eq. 10 + label update (labels updated in place)."""
+    a = _lookup_args(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count)
+    _check(lib().clo_lookup_update(*a, _stream(stream)), "clo_lookup_update")
 
 
 # ---------------------------------------------------------------- offline plan
@@ -286,6 +293,35 @@ def clo_hybrid_decode_attn(q: torch.Tensor, cbK: Optional[torch.Tensor],
     fp32 (optional); workspace: a CUDA uint8 tensor of at least
     clo_hybrid_workspace_size(...) bytes.
     """
+    a = _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_hybrid_decode_attn(
+        *a, ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "clo_hybrid_decode_attn")
+
+
+def clo_hybrid_decode_attn_lookup(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace,
+                                  q_next, labels_next, w_q_next, tau_next, persist_mask_next,
+                                  flag_next, sim_next, miss_list_next, miss_count_next,
+                                  lse=None, err_flag=None, scale=None, num_ctas: int = 0,
+                                  events=None, stream=None):
+    """clo_hybrid_decode_attn for this layer and clo_lookup_update for the next
+    layer (same B, Hq, Hkv) in one launch sequence; the results equal the two
+    separate calls."""
+    a = _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale)
+    b = _lookup_args(q_next, labels_next, w_q_next, tau_next, persist_mask_next, flag_next,
+                     sim_next, miss_list_next, miss_count_next)
+    if b[5:9] != a[11:15]:
+        raise CloError("the next layer's lookup must have this layer's B, Hq, Hkv, d",
+                       CLO_ERR_INVALID_ARG)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_hybrid_decode_attn_lookup(
+        *a, b[0], b[1], b[2], b[3], b[4], b[9], b[10], b[11], b[12],
+        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "clo_hybrid_decode_attn_lookup")
+
+
+def _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale):
     pq = _dev(q, "q", torch.float16, 3)
     B, Hq, d = q.shape
     Np = 0 if persist_ids is None else persist_ids.numel()
@@ -309,12 +345,8 @@ def clo_hybrid_decode_attn(q: torch.Tensor, cbK: Optional[torch.Tensor],
         raise CloError("out / lse shapes do not match q", CLO_ERR_INVALID_ARG)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    opts = _opts(num_ctas, events)
-    _check(lib().clo_hybrid_decode_attn(
-        pq, pcbk, pcbv, pidx, k, C, ppk, ppv, ppid, Np, T, B, Hq, Hkv, d, float(scale),
-        pout, plse, pws, workspace.numel(), perr,
-        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
-        "clo_hybrid_decode_attn")
+    return (pq, pcbk, pcbv, pidx, k, C, ppk, ppv, ppid, Np, T, B, Hq, Hkv, d, float(scale),
+            pout, plse, pws, workspace.numel(), perr)
 
 
 def clo_paged_decode_attn(q: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor,

@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "clo_device.cuh"
+#include "clo_lookup.cuh"
 
 namespace clo {
 
@@ -646,8 +647,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     int* gsm = reinterpret_cast<int*>(ms.o + ATTN_WARPS * o.G * OSTRIDE);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_launch_dependents();
+    // Dependents may start only once this grid has passed its own wait, so a
+    // dependent's code before its wait sees everything written before this
+    // kernel (the merge kernel runs a fused lookup there).
     pdl_wait();
+    pdl_launch_dependents();
     // With a static layout (hybrid) the CTA ranges and the addresses of
     // contiguous Persistent Cache tiles need no shared state, so the first of
     // those copies are issued before the CTA reads persist_ids; the id round
@@ -812,7 +816,8 @@ constexpr int MERGE_UNROLL = 8;                                 // independent p
 
 template <class Geo>
 __global__ void __launch_bounds__(MERGE_THREADS, 1)
-    attn_merge_kernel(const Geo geo, const AttnOut o, int C, int hpb) {
+    attn_merge_kernel(const Geo geo, const AttnOut o, int C, int hpb, int n_merge,
+                      const LookupParams lk, int lk_first) {
     extern __shared__ __align__(16) uint8_t msmem[];
     // Block (x, y) merges query heads [y * hpb, (y + 1) * hpb) of one cut token set.
     const int G = o.G;
@@ -825,6 +830,18 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
     int* gsm = reinterpret_cast<int*>(Og + 2 * MERGE_THREADS);
 
     pdl_launch_dependents();
+    if (static_cast<int>(blockIdx.x) >= n_merge) {
+        // Past the merge blocks: one cluster at the end of row 0 runs the
+        // next layer's lookup; the other blocks only pad the grid to whole
+        // clusters.  The lookup reads nothing the attention writes, and the
+        // main kernel let this grid start only after its own dependency wait,
+        // so it needs no wait of its own and overlaps the main kernel's tail.
+        if (lk.B > 0 && static_cast<int>(blockIdx.x) >= lk_first && blockIdx.y == 0) {
+            __shared__ int lk_misses;
+            lookup_cluster<MERGE_THREADS / 32>(lk, msmem, &lk_misses);
+        }
+        return;
+    }
     // Static layouts (hybrid): block s handles token set s if CTA boundaries
     // cut it; the test needs no memory, so blocks with nothing to merge leave
     // at once.  Dynamic layouts (paged): block (part, i) looks at the boundary
@@ -1053,7 +1070,8 @@ static size_t merge_smem_bytes(int /*G*/, size_t geo_ints) {
 template <class Geo>
 static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_host_bound,
                                    size_t geo_ints, int S, void* workspace, size_t ws_bytes,
-                                   const clo_attn_opts* opts, cudaStream_t stream) {
+                                   const clo_attn_opts* opts, cudaStream_t stream,
+                                   const LookupParams* lookup = nullptr) {
     if (!prepare_kernel(reinterpret_cast<const void*>(attn_split_kernel<Geo>), SMEM_LIMIT) ||
         !prepare_kernel(reinterpret_cast<const void*>(attn_merge_kernel<Geo>), MERGE_SMEM_LIMIT))
         return CLO_ERR_CUDA;
@@ -1089,17 +1107,34 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
         return CLO_ERR_CUDA;
     if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
+    const int merge_blocks =
+        C < 2 ? 0 : (Geo::kStaticLayout ? geo.num_segments() : Geo::kParts * (C - 1));
+    // All heads in one block when every cut token set has few enough partials
+    // for one round of loads per thread group; else one head per block.
+    int hpb = o.G;
     if (C >= 2) {
-        const int merge_blocks = Geo::kStaticLayout ? geo.num_segments() : Geo::kParts * (C - 1);
-        // All heads in one block when every cut token set has few enough
-        // partials for one round of loads per thread group; else one head per block.
         const long long most = geo.max_partials_host(C);
         const int ngrp_all = MERGE_THREADS / (o.G * MERGE_ITEMS);
-        const int hpb = most <= static_cast<long long>(ngrp_all) * MERGE_UNROLL ? o.G : 1;
-        if (launch_pdl(attn_merge_kernel<Geo>, dim3(merge_blocks, o.G / hpb), dim3(MERGE_THREADS),
-                       msmem, stream, geo, o, C, hpb) != cudaSuccess)
-            return CLO_ERR_CUDA;
+        hpb = most <= static_cast<long long>(ngrp_all) * MERGE_UNROLL ? o.G : 1;
     }
+    LookupParams none{};
+    if (lookup == nullptr) {
+        if (merge_blocks > 0 &&
+            launch_pdl(attn_merge_kernel<Geo>, dim3(merge_blocks, o.G / hpb), dim3(MERGE_THREADS),
+                       msmem, stream, geo, o, C, hpb, merge_blocks, none, merge_blocks) !=
+                cudaSuccess)
+            return CLO_ERR_CUDA;
+        return CLO_OK;
+    }
+    // The next layer's lookup rides in the merge launch: whole clusters of
+    // LK_CLUSTER blocks, the lookup's cluster last.
+    const int lk_first = (merge_blocks + LK_CLUSTER - 1) / LK_CLUSTER * LK_CLUSTER;
+    const size_t lsmem = std::max(msmem, static_cast<size_t>(lookup_smem_bytes(lookup->B, lookup->Hkv)));
+    if (lsmem > static_cast<size_t>(MERGE_SMEM_LIMIT)) return CLO_ERR_UNSUPPORTED;
+    if (launch_pdl_cluster(attn_merge_kernel<Geo>, dim3(lk_first + LK_CLUSTER, o.G / hpb),
+                           dim3(MERGE_THREADS), lsmem, stream, LK_CLUSTER, geo, o, C, hpb,
+                           merge_blocks, *lookup, lk_first) != cudaSuccess)
+        return CLO_ERR_CUDA;
     return CLO_OK;
 }
 
@@ -1115,14 +1150,13 @@ extern "C" size_t clo_paged_workspace_size(int B, int Hq, int Hkv, int d, int nu
     return workspace_bytes(B, Hq, Hkv, d, num_ctas);
 }
 
-extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
-                                             const clo_half* cbV, const int32_t* idx, int k, int C,
-                                             const clo_half* pK, const clo_half* pV,
-                                             const int32_t* persist_ids, int Np, int T, int B,
-                                             int Hq, int Hkv, int d, float scale, clo_half* out,
-                                             float* lse, void* workspace, size_t ws_bytes,
-                                             int32_t* err_flag, const clo_attn_opts* opts,
-                                             cudaStream_t stream) {
+static clo_status hybrid_attention(const clo_half* q, const clo_half* cbK, const clo_half* cbV,
+                                   const int32_t* idx, int k, int C, const clo_half* pK,
+                                   const clo_half* pV, const int32_t* persist_ids, int Np, int T,
+                                   int B, int Hq, int Hkv, int d, float scale, clo_half* out,
+                                   float* lse, void* workspace, size_t ws_bytes, int32_t* err_flag,
+                                   const clo_attn_opts* opts, cudaStream_t stream,
+                                   const LookupParams* lookup) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Np < 0 || Np > Hkv)
         return CLO_ERR_INVALID_ARG;
     if (B == 0) return CLO_OK;  // empty batch: nothing to compute
@@ -1174,7 +1208,42 @@ extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* 
     o.Hq = Hq;
     o.G = G;
     return launch_attention(geo, o, N, HybridGeo::smem_ints(Hkv, B), B * Hkv, workspace,
-                            ws_bytes, opts, stream);
+                            ws_bytes, opts, stream, lookup);
+}
+
+extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
+                                             const clo_half* cbV, const int32_t* idx, int k, int C,
+                                             const clo_half* pK, const clo_half* pV,
+                                             const int32_t* persist_ids, int Np, int T, int B,
+                                             int Hq, int Hkv, int d, float scale, clo_half* out,
+                                             float* lse, void* workspace, size_t ws_bytes,
+                                             int32_t* err_flag, const clo_attn_opts* opts,
+                                             cudaStream_t stream) {
+    return hybrid_attention(q, cbK, cbV, idx, k, C, pK, pV, persist_ids, Np, T, B, Hq, Hkv, d,
+                            scale, out, lse, workspace, ws_bytes, err_flag, opts, stream, nullptr);
+}
+
+extern "C" clo_status clo_hybrid_decode_attn_lookup(
+    const clo_half* q, const clo_half* cbK, const clo_half* cbV, const int32_t* idx, int k, int C,
+    const clo_half* pK, const clo_half* pV, const int32_t* persist_ids, int Np, int T, int B,
+    int Hq, int Hkv, int d, float scale, clo_half* out, float* lse, void* workspace,
+    size_t ws_bytes, int32_t* err_flag, const clo_half* q_next, clo_half* labels_next,
+    const float* w_q_next, const float* tau_next, const uint8_t* persist_mask_next,
+    uint8_t* flag_next, float* sim_next, int32_t* miss_list_next, int32_t* miss_count_next,
+    const clo_attn_opts* opts, cudaStream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return CLO_ERR_INVALID_ARG;
+    if (miss_count_next == nullptr || !aligned(miss_count_next, 4)) return CLO_ERR_INVALID_ARG;
+    if (B == 0)  // nothing to attend to or look up: only the miss count is written
+        return cudaMemsetAsync(miss_count_next, 0, sizeof(int32_t), stream) == cudaSuccess
+                   ? CLO_OK
+                   : CLO_ERR_CUDA;
+    LookupParams lk;
+    const clo_status st = make_lookup_params(q_next, labels_next, w_q_next, tau_next,
+                                             persist_mask_next, B, Hq, Hkv, d, flag_next,
+                                             sim_next, miss_list_next, miss_count_next, lk);
+    if (st != CLO_OK) return st;
+    return hybrid_attention(q, cbK, cbV, idx, k, C, pK, pV, persist_ids, Np, T, B, Hq, Hkv, d,
+                            scale, out, lse, workspace, ws_bytes, err_flag, opts, stream, &lk);
 }
 
 extern "C" clo_status clo_paged_decode_attn(const clo_half* q, const clo_half* kc,

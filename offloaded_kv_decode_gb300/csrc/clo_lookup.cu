@@ -1,32 +1,15 @@
 // clo_lookup.cu -- per-head thresholds (CLO Eqs. 7-9) and the fused head-wise
 // approximate-cache lookup + query-label update (CLO section 2, Eq. 10,
-// section 3 Fig. 7), for sm_103a.
-//
-// The lookup is one launch of a single 8-CTA thread-block cluster.  Each CTA
-// takes a contiguous share of the (batch row, KV head) groups; one warp scores
-// one group: every lane holds 4 of the 128 dimensions of each of the G query
-// heads, so q and the labels are read from HBM exactly once with 8-byte loads,
-// and the three dot products per head are finished with warp shuffles.  On a
-// miss the same registers are written back as the new labels.  The compact
-// miss list is made deterministic (ascending b*Hkv+g) without a second launch
-// or any global scratch: after a cluster barrier every CTA reads the miss
-// counts of the lower-ranked CTAs from their shared memory (DSMEM) and writes
-// its own misses at that offset.
-#include <cooperative_groups.h>
-
-#include "clo_device.cuh"
-
-namespace cg = cooperative_groups;
+// section 3 Fig. 7), for sm_103a.  The lookup is one launch of a single
+// 8-CTA thread-block cluster running lookup_cluster (clo_lookup.cuh).
+#include "clo_lookup.cuh"
 
 namespace clo {
 
-constexpr int LK_CLUSTER = 8;
 // 4 warps per CTA: small enough (with <= 64 registers per thread) to be
 // resident next to an attention CTA, so a lookup can overlap attention.
 constexpr int LK_THREADS = 128;
 constexpr int LK_WARPS = LK_THREADS / 32;
-constexpr int LK_MAX_G = 8;
-constexpr int LK_MAX_GROUPS = 65536;
 constexpr float PI_F = 3.14159265358979323846f;
 
 __global__ void thresholds_kernel(const float* __restrict__ s, int n_kv, int group, float eta,
@@ -44,131 +27,13 @@ __global__ void thresholds_kernel(const float* __restrict__ s, int n_kv, int gro
     tau[g] = cosf(theta);
 }
 
-struct LookupParams {
-    const clo_half* q;
-    clo_half* labels;
-    const float* w;
-    const float* tau;
-    const uint8_t* pmask;
-    uint8_t* flag;
-    float* sim;
-    int32_t* miss_list;
-    int32_t* miss_count;
-    int B, Hq, Hkv, G;
-};
-
-__device__ __forceinline__ float2 h2f(uint32_t v) {
-    __half2 h = *reinterpret_cast<__half2*>(&v);
-    return __half22float2(h);
-}
-
 __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS, 8)
     lookup_update_kernel(const LookupParams p) {
     extern __shared__ uint8_t miss_sm[];  // miss bit of each group of this CTA
     __shared__ int cta_misses;
     pdl_launch_dependents();
     pdl_wait();
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = static_cast<int>(cluster.block_rank());
-    const int ngroups = p.B * p.Hkv;
-    const int g0 = static_cast<int>(static_cast<long long>(ngroups) * rank / LK_CLUSTER);
-    const int g1 = static_cast<int>(static_cast<long long>(ngroups) * (rank + 1) / LK_CLUSTER);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    for (int gi = g0 + warp; gi < g1; gi += LK_WARPS) {
-        const int b = gi / p.Hkv;
-        const int g = gi - b * p.Hkv;
-        const size_t base = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G) * 128 +
-                            static_cast<size_t>(lane) * 4;
-        // Every load of the group is issued before the first use.
-        uint2 qv[LK_MAX_G], lv[LK_MAX_G];
-        float wv[LK_MAX_G];
-#pragma unroll
-        for (int j = 0; j < LK_MAX_G; ++j) {
-            if (j < p.G) {
-                qv[j] = *reinterpret_cast<const uint2*>(p.q + base + j * 128);
-                lv[j] = *reinterpret_cast<const uint2*>(p.labels + base + j * 128);
-                wv[j] = __ldg(p.w + g * p.G + j);
-            }
-        }
-        const float tau_g = __ldg(p.tau + g);
-        const bool persistent = p.pmask != nullptr && __ldg(p.pmask + g) != 0;
-        float sw = 0.f, swc = 0.f, sc = 0.f;
-#pragma unroll
-        for (int j = 0; j < LK_MAX_G; ++j) {
-            if (j < p.G) {
-                const float2 qa = h2f(qv[j].x), qb = h2f(qv[j].y);
-                const float2 la = h2f(lv[j].x), lb = h2f(lv[j].y);
-                float dot = qa.x * la.x;
-                dot = fmaf(qa.y, la.y, dot);
-                dot = fmaf(qb.x, lb.x, dot);
-                dot = fmaf(qb.y, lb.y, dot);
-                float qq = qa.x * qa.x;
-                qq = fmaf(qa.y, qa.y, qq);
-                qq = fmaf(qb.x, qb.x, qq);
-                qq = fmaf(qb.y, qb.y, qq);
-                float ll = la.x * la.x;
-                ll = fmaf(la.y, la.y, ll);
-                ll = fmaf(lb.x, lb.x, ll);
-                ll = fmaf(lb.y, lb.y, ll);
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    dot += __shfl_xor_sync(FULL_MASK, dot, off);
-                    qq += __shfl_xor_sync(FULL_MASK, qq, off);
-                    ll += __shfl_xor_sync(FULL_MASK, ll, off);
-                }
-                const float c = (qq > 0.f && ll > 0.f) ? dot / (sqrtf(qq) * sqrtf(ll)) : 0.f;
-                const float w = wv[j];
-                sw += w;
-                swc = fmaf(w, c, swc);
-                sc += c;
-            }
-        }
-        const float s = (sw != 0.f) ? swc / sw : sc / static_cast<float>(p.G);  // Eq. 10
-        uint8_t f;
-        if (persistent) {
-            f = 2;  // persistent: always resident, never looked up
-        } else if (s >= tau_g) {
-            f = 0;  // hit: keep the label
-        } else {
-            f = 1;  // miss: the whole KV head is replaced, labels <- current queries
-#pragma unroll
-            for (int j = 0; j < LK_MAX_G; ++j)
-                if (j < p.G) *reinterpret_cast<uint2*>(p.labels + base + j * 128) = qv[j];
-        }
-        if (lane == 0) {
-            p.flag[gi] = f;
-            p.sim[gi] = s;
-            miss_sm[gi - g0] = (f == 1);
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int cnt = 0;
-        for (int i = lane; i < g1 - g0; i += 32) cnt += miss_sm[i];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(FULL_MASK, cnt, off);
-        if (lane == 0) cta_misses = cnt;
-    }
-    cluster.sync();
-    if (warp == 0) {
-        int pos = 0;
-        for (int r = 0; r < rank; ++r) pos += *cluster.map_shared_rank(&cta_misses, r);
-        for (int i0 = 0; i0 < g1 - g0; i0 += 32) {
-            const int i = i0 + lane;
-            const bool m = (i < g1 - g0) && miss_sm[i] != 0;
-            const unsigned bal = __ballot_sync(FULL_MASK, m);
-            if (m) p.miss_list[pos + __popc(bal & ((1u << lane) - 1u))] = g0 + i;
-            pos += __popc(bal);
-        }
-        if (rank == LK_CLUSTER - 1 && lane == 0) *p.miss_count = pos;
-    }
-    cluster.sync();  // keep every CTA's shared memory alive until all reads are done
-}
-
-static bool aligned(const void* p, size_t a) {
-    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+    lookup_cluster<LK_WARPS>(p, miss_sm, &cta_misses);
 }
 
 }  // namespace clo
@@ -194,25 +59,19 @@ extern "C" clo_status clo_lookup_update(const clo_half* q, clo_half* labels, con
                                         int Hq, int Hkv, int d, uint8_t* flag, float* sim,
                                         int32_t* miss_list, int32_t* miss_count,
                                         cudaStream_t stream) {
-    if (miss_count == nullptr || !aligned(miss_count, 4)) return CLO_ERR_INVALID_ARG;
+    if (miss_count == nullptr || (reinterpret_cast<uintptr_t>(miss_count) % 4) != 0)
+        return CLO_ERR_INVALID_ARG;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return CLO_ERR_INVALID_ARG;
     if (B == 0) {  // nothing to look up: only the miss count is written
         return cudaMemsetAsync(miss_count, 0, sizeof(int32_t), stream) == cudaSuccess
                    ? CLO_OK
                    : CLO_ERR_CUDA;
     }
-    if (q == nullptr || labels == nullptr || w_q == nullptr || tau_kv == nullptr ||
-        flag == nullptr || sim == nullptr || miss_list == nullptr)
-        return CLO_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(labels, 16) || !aligned(w_q, 4) || !aligned(tau_kv, 4) ||
-        !aligned(sim, 4) || !aligned(miss_list, 4))
-        return CLO_ERR_INVALID_ARG;
-    const int G = Hq / Hkv;
-    if (d != 128 || G > LK_MAX_G) return CLO_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * Hkv > LK_MAX_GROUPS) return CLO_ERR_UNSUPPORTED;
-    LookupParams p{q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count,
-                   B, Hq, Hkv, G};
-    const int per_cta = (B * Hkv + LK_CLUSTER - 1) / LK_CLUSTER;
+    LookupParams p;
+    const clo_status st = make_lookup_params(q, labels, w_q, tau_kv, persist_mask, B, Hq, Hkv, d,
+                                             flag, sim, miss_list, miss_count, p);
+    if (st != CLO_OK) return st;
+    const int per_cta = lookup_smem_bytes(B, Hkv);
     if (!prepare_kernel(reinterpret_cast<const void*>(lookup_update_kernel), per_cta))
         return CLO_ERR_CUDA;
     return launch_pdl(lookup_update_kernel, dim3(LK_CLUSTER), dim3(LK_THREADS),

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 13, names
+    assert len(names) == 14, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -143,3 +143,17 @@ def test_fill_rejects(L):
     assert _fill(L, d=64) == clo.CLO_ERR_UNSUPPORTED
     assert _fill(L, k=0) == clo.CLO_OK                           # nothing to move: no launch
     assert _fill(L, B=0) == clo.CLO_OK
+
+
+def test_fused_lookup_rejects(L):
+    # The next layer's lookup arguments are checked before anything launches.
+    def fused(q_next=FAKE, miss_count=FAKE, B=1, Hq=32, Hkv=8):
+        return L.clo_hybrid_decode_attn_lookup(
+            FAKE, FAKE, FAKE, FAKE, 10, 100, FAKE, FAKE, FAKE, 2, 50, B, Hq, Hkv, 128, 0.088,
+            FAKE, None, FAKE, 1 << 30, None,
+            q_next, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, miss_count, None, None)
+    assert fused(q_next=None) == clo.CLO_ERR_INVALID_ARG
+    assert fused(q_next=FAKE + 2) == clo.CLO_ERR_INVALID_ARG
+    assert fused(miss_count=None) == clo.CLO_ERR_INVALID_ARG
+    assert fused(Hq=30) == clo.CLO_ERR_INVALID_ARG
+    assert fused(B=9000) == clo.CLO_ERR_UNSUPPORTED
