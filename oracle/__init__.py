@@ -74,6 +74,8 @@ class Oracle:
         lib.oracle_fill_cache_buffer.restype = _I
         lib.oracle_plan_persistent.argtypes = [_P, _P, _I, _I, _D, _D, _D, _D, _P, _P, _P, _P]
         lib.oracle_plan_persistent.restype = _I
+        lib.oracle_topk_retrieve.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _P]
+        lib.oracle_topk_retrieve.restype = _I
         self.lib = lib
 
     # -- helpers ----------------------------------------------------------
@@ -238,6 +240,19 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"oracle_plan_persistent rc={rc}")
         return dict(D=D, n_p=int(n_p[0]), n_persist=n_persist[:L].copy(), persist_ids=ids[:L].copy())
+
+    def topk_retrieve(self, q, K, k: int) -> np.ndarray:
+        """q [B][Hq][d], K [B][Hkv][T][d] fp16 -> idx int32 [B][Hkv][k]: per KV
+        head the k tokens with the largest (sum of the group's q) . K_t,
+        ties to the lower token, ascending."""
+        q, K = self._u16(q), self._u16(K)
+        B, Hq, d = q.shape
+        Hkv, T = K.shape[1], K.shape[2]
+        idx = np.zeros((B, Hkv, max(k, 1)), dtype=np.int32)
+        rc = self.lib.oracle_topk_retrieve(_ptr(q), _ptr(K), B, Hq, Hkv, T, d, int(k), _ptr(idx))
+        if rc != OK:
+            raise ValueError(f"oracle_topk_retrieve rc={rc}")
+        return idx[:, :, :k].copy()
 
 
 _default = None

@@ -37,6 +37,11 @@
  *                         (Eq. 12); the heads of layer l kept resident,
  *                         N_persist^l = max(N_hard^l - N_p, 0) with N_hard^l the
  *                         heads of the layer with D_i > 0 (Eq. 13).
+ *   oracle_topk_retrieve  CLO page, section 2, Eq. 6 (the qk-score ranking of
+ *                         the keys does not depend on |q|) and the top-k
+ *                         retrieval stage of the decode flow (section 3): the
+ *                         k keys of each KV head with the largest score
+ *                         against the group's queries.
  *   oracle_fill_cache_buffer  CLO page, section 3, Fig. 7 (an update writes
  *                         the new KV data straight to its final position, no
  *                         staging buffer) and section 2 (only missed heads
@@ -60,6 +65,11 @@
  *   - Eq. 12 as printed divides T_comp by B_link * mem_head, which is not
  *     dimensionless; the count of heads one layer can prefetch is taken as
  *     T_comp * B_link / mem_head, rounded down.
+ *   - Top-k retrieval: the page names HATA hash scoring but gives no algorithm;
+ *     the exact ranking is used.  A KV head's score of key t is the dot
+ *     product of the sum of its G query vectors with K_t (the group's summed
+ *     qk-score); the k largest are taken, equal scores at the cut going to
+ *     the lower token index, and listed in ascending token order.
  *   - Of the hard heads (D_i > 0, strictly) of a layer, the N_persist^l with
  *     the largest D_i are kept resident (the rest are prefetched); equal D_i
  *     are taken in increasing head order.
@@ -400,5 +410,61 @@ int oracle_plan_persistent(const double* tau, const double* s_hat, int L, int Hk
             persist_ids[(size_t)l * Hkv + j] = best;
         }
     }
+    return ORACLE_OK;
+}
+
+/* Top-k retrieval by exact qk-score.
+ *   q    [B][Hq][d]       queries (G = Hq / Hkv per KV head)
+ *   K    [B][Hkv][T][d]   all keys of each KV head
+ *   idx  [B][Hkv][k]      output: the selected tokens, ascending
+ * score(t) = (sum of the group's q_h) . K_t in fp64; the k largest scores,
+ * ties at the cut to the lower token index. */
+static const double* g_topk_scores; /* for the comparator below */
+
+static int by_score_then_index(const void* a, const void* b) {
+    int i = *(const int*)a, j = *(const int*)b;
+    double si = g_topk_scores[i], sj = g_topk_scores[j];
+    if (si > sj) return -1;
+    if (si < sj) return 1;
+    return i < j ? -1 : (i > j);
+}
+
+static int by_index(const void* a, const void* b) {
+    int i = *(const int*)a, j = *(const int*)b;
+    return (i > j) - (i < j);
+}
+
+int oracle_topk_retrieve(const uint16_t* q, const uint16_t* K, int B, int Hq, int Hkv, int T,
+                         int d, int k, int32_t* idx) {
+    if (B < 0 || Hkv <= 0 || Hq % Hkv != 0 || T < 0 || d <= 0 || k < 0 || k > T)
+        return ORACLE_BAD_ARG;
+    int G = Hq / Hkv;
+    double* qs = (double*)malloc((size_t)d * sizeof(double));
+    double* sc = (double*)malloc((size_t)(T ? T : 1) * sizeof(double));
+    int* order = (int*)malloc((size_t)(T ? T : 1) * sizeof(int));
+    if (!qs || !sc || !order) { free(qs); free(sc); free(order); return ORACLE_BAD_ARG; }
+    for (int b = 0; b < B; ++b) {
+        for (int g = 0; g < Hkv; ++g) {
+            for (int i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < G; ++j)
+                    acc += oracle_half_to_double(q[((size_t)b * Hq + (size_t)g * G + j) * d + i]);
+                qs[i] = acc;
+            }
+            const uint16_t* Kh = K + (((size_t)b * Hkv + g) * (size_t)T) * d;
+            for (int t = 0; t < T; ++t) {
+                double dot = 0.0;
+                for (int i = 0; i < d; ++i)
+                    dot += qs[i] * oracle_half_to_double(Kh[(size_t)t * d + i]);
+                sc[t] = dot;
+                order[t] = t;
+            }
+            g_topk_scores = sc;
+            qsort(order, (size_t)T, sizeof(int), by_score_then_index);
+            qsort(order, (size_t)k, sizeof(int), by_index);
+            memcpy(idx + ((size_t)b * Hkv + g) * (size_t)k, order, (size_t)k * sizeof(int32_t));
+        }
+    }
+    free(qs); free(sc); free(order);
     return ORACLE_OK;
 }

@@ -619,6 +619,61 @@ def pin_plan_invariants(orc):
                 assert 1 in kept and kept.index(1) < kept.index(5)
 
 
+# -- top-k retrieval (CLO page, section 2, Eq. 6; the decode flow's top-k
+#    retrieval stage), exact ranking by the group's summed qk-score ----------
+
+def pin_topk_worked_example(orc):
+    """Two query heads [1, 0] and [0, 1] share one KV head, so the score of a
+    key is its coordinate sum: 2, 1, 3, -2, 2 for the five keys below."""
+    q = _h([[[1, 0], [0, 1]]])
+    K = _h([[[[1, 1], [2, -1], [0, 3], [-1, -1], [1, 1]]]])
+    for k, want in ((5, [0, 1, 2, 3, 4]), (3, [0, 2, 4]), (2, [0, 2]), (1, [2]), (0, [])):
+        got = orc.topk_retrieve(q, K, k)
+        assert got.shape == (1, 1, k) and got[0, 0].tolist() == want, (k, got)
+
+
+def pin_topk_is_the_best_set(orc):
+    """On random inputs (several KV heads, GQA 4) the selected set beats every
+    unselected key, in float64 scores computed here with torch, and other
+    groups' queries do not matter."""
+    rng = _rng(71)
+    B, Hkv, G, T, d, k = 2, 3, 4, 97, 32, 13
+    q = _f16(rng, (B, Hkv * G, d))
+    K = _f16(rng, (B, Hkv, T, d))
+    idx = orc.topk_retrieve(q, K, k)
+    for b in range(B):
+        for g in range(Hkv):
+            qs = torch.from_numpy(q[b, g * G:(g + 1) * G].astype(np.float64)).sum(0)
+            sc = (torch.from_numpy(K[b, g].astype(np.float64)) @ qs).numpy()
+            sel = idx[b, g].tolist()
+            assert sel == sorted(set(sel)) and len(sel) == k
+            rest = np.setdiff1d(np.arange(T), sel)
+            assert sc[sel].min() > sc[rest].max(), (b, g)
+    q2 = q.copy()
+    q2[:, :G] = _f16(rng, (B, G, d), scale=50.0)   # only group 0's queries change
+    idx2 = orc.topk_retrieve(q2, K, k)
+    assert np.array_equal(idx2[:, 1:], idx[:, 1:])
+
+
+def pin_topk_norm_invariance(orc):
+    """Eq. 6: scaling every query of the group by the same positive factor
+    (powers of two, exact in binary16) leaves the selection unchanged."""
+    rng = _rng(72)
+    q = _f16(rng, (1, 8, 64))
+    K = _f16(rng, (1, 2, 150, 64))
+    base = orc.topk_retrieve(q, K, 15)
+    for f in (0.25, 4.0):
+        assert np.array_equal(orc.topk_retrieve((q.astype(np.float32) * f).astype(np.float16), K, 15),
+                              base)
+
+
+def pin_topk_ties_to_lower_token(orc):
+    """Identical keys tie; the cut takes the lower token indices."""
+    q = _h([[[1, 2]]])
+    K = _h([[[[1, 1]] * 6 + [[5, 5]] * 2]])
+    assert orc.topk_retrieve(q, K, 4)[0, 0].tolist() == [0, 1, 6, 7]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -59,6 +59,13 @@ MUTANTS = [
      "if (best < 0 || D[at] < D[(size_t)l * Hkv + best]) best = i;"),
     ("tie goes to the higher head", "if (best < 0 || D[at] > D[(size_t)l * Hkv + best]) best = i;",
      "if (best < 0 || D[at] >= D[(size_t)l * Hkv + best]) best = i;"),
+    ("top-k one query of the group", "acc += oracle_half_to_double(q[((size_t)b * Hq + (size_t)g * G + j) * d + i]);",
+     "acc += oracle_half_to_double(q[((size_t)b * Hq + (size_t)g * G) * d + i]);"),
+    ("top-k strided grouping", "acc += oracle_half_to_double(q[((size_t)b * Hq + (size_t)g * G + j) * d + i]);",
+     "acc += oracle_half_to_double(q[((size_t)b * Hq + (size_t)j * Hkv + g) * d + i]);"),
+    ("top-k smallest scores", "if (si > sj) return -1;", "if (si < sj) return -1;"),
+    ("top-k ties to higher token", "return i < j ? -1 : (i > j);", "return i > j ? -1 : (i < j);"),
+    ("top-k output not ascending", "qsort(order, (size_t)k, sizeof(int), by_index);", ""),
     ("fill last row dropped", "for (int j = 0; j < k; ++j) {\n            size_t sel",
      "for (int j = 0; j < k - 1; ++j) {\n            size_t sel"),
 ]
