@@ -433,6 +433,76 @@ class FillWorkload:
                 "l2": "two buffer sets alternate; consecutive calls read and write disjoint rows"}
 
 
+class TopkWorkload:
+    """Top-k retrieval: every KV head ranks all T keys of the base layer
+    against its query group and keeps the top k.  Two buffer sets alternate
+    (each set's keys are larger than L2)."""
+    kind = "topk"
+    kernel = "topk_score_kernel"
+    kernel_src = "clo_topk.cu"
+
+    def __init__(self, name, dev, rank: int, batch: int = 0):
+        import torch
+        import offloaded_kv_decode_gb300 as clo
+
+        self.name = name
+        self.clo, self.torch = clo, torch
+        cfg = wl.CONFIGS[wl.TOPK_CONFIGS[name]]
+        if batch:
+            cfg = dataclasses.replace(cfg, B=batch)
+        self.cfg = cfg if rank == 0 else dataclasses.replace(cfg, seed=cfg.seed + 1000 * rank)
+        self.L, self.n_inst, self.phases = 1, 2, 2
+        self.inst = []
+        for i in range(self.n_inst):
+            li = i + 1000 * rank
+            q, _ = wl.queries_and_labels(self.cfg, li, dev)
+            K, V = wl.full_kv(self.cfg, li, dev)
+            del V
+            self.inst.append(dict(q=q, K=K, idx=torch.empty((cfg.B, cfg.Hkv, cfg.k),
+                                                            dtype=torch.int32, device=dev)))
+        self.ws = torch.empty(clo.clo_topk_workspace_size(cfg.B, cfg.Hkv, cfg.T),
+                              dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def attn_bytes_per_launch(self) -> int:
+        """The scoring kernel's algorithmic reads: every key and the queries."""
+        c = self.cfg
+        return c.B * c.Hkv * c.T * c.d * HALF + c.B * c.Hq * c.d * HALF
+
+    def bytes_per_step(self) -> int:
+        c = self.cfg
+        return self.attn_bytes_per_launch() + c.B * c.Hkv * c.k * 4
+
+    def launches_per_step(self) -> int:
+        return 2  # scoring, selection
+
+    def launch(self, step: int, attn_events=None):
+        it = self.inst[step % self.n_inst]
+        self.clo.clo_topk_retrieve(it["q"], it["K"], self.cfg.k, it["idx"], self.ws,
+                                   events=None if attn_events is None else attn_events[0])
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.h_q = [it["q"].cpu().pin_memory() for it in self.inst]
+        self.h_idx = [torch.empty_like(it["idx"], device="cpu").pin_memory() for it in self.inst]
+        c = self.cfg
+        self.e2e_h2d = c.B * c.Hq * c.d * HALF
+        self.e2e_d2h = c.B * c.Hkv * c.k * 4
+
+    def e2e_step(self, step: int):
+        j = step % self.n_inst
+        self.inst[j]["q"].copy_(self.h_q[j], non_blocking=True)
+        self.launch(step)
+        self.h_idx[j].copy_(self.inst[j]["idx"], non_blocking=True)
+
+    def config(self) -> dict:
+        c = self.cfg
+        return {"workload": self.name, "base": c.name, "batch": c.B, "q_heads": c.Hq,
+                "kv_heads": c.Hkv, "head_dim": c.d, "keys_per_head": c.T, "top_k": c.k,
+                "score": "sum of the group's queries . K_t, fp32",
+                "l2": f"two buffer sets of {c.B * c.Hkv * c.T * c.d * HALF / 2**20:.0f} MiB of keys alternate"}
+
+
 def measure_h2d_gbs(torch, nbytes: int = 512 * 2 ** 20, reps: int = 5) -> float:
     """Pinned host-to-device copy bandwidth (GB/s), best of reps."""
     h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
@@ -491,6 +561,19 @@ def oracle_sample(name: str):
                          n * small.d * HALF * 2 + extra + 2 * G * small.d * HALF))
         desc = (f"one batch row of {cfg.name} (all {cfg.Hkv} KV heads: lookup, then attention "
                 f"over {cfg.Np} persistent x {cfg.T} and {cfg.Hkv - cfg.Np} x {cfg.k} indexed rows)")
+    elif name in wl.TOPK_CONFIGS:
+        cfg = wl.CONFIGS[wl.TOPK_CONFIGS[name]]
+        small = dataclasses.replace(cfg, B=1)
+        q, _ = wl.queries_and_labels(small, 0)
+        K, _ = wl.full_kv(small, 0)
+        qn, Kn = q.numpy(), K.numpy()
+        for g in range(small.Hkv):
+            G = small.G
+            jobs.append((lambda g=g: orc.topk_retrieve(qn[:, g * G:(g + 1) * G], Kn[:, g:g + 1],
+                                                        small.k),
+                         small.T * small.d * HALF + G * small.d * HALF))
+        desc = (f"one batch row of {name} ({small.Hkv} KV heads x {small.T} keys, k = {small.k}, "
+                f"fp64 scores and a full sort)")
     elif name in wl.FILL_CONFIGS:
         base, _ = wl.FILL_CONFIGS[name]
         cfg = wl.CONFIGS[base]
@@ -682,6 +765,8 @@ def run_ours(args):
         W = HybridWorkload(cfg, dev, rank, args.replicas, schedule=args.lookup_schedule)
     elif args.workload in wl.FILL_CONFIGS:
         W = FillWorkload(args.workload, dev, rank, args.batch)
+    elif args.workload in wl.TOPK_CONFIGS:
+        W = TopkWorkload(args.workload, dev, rank, args.batch)
     else:
         pc = wl.PAGED_CONFIGS[args.workload]
         if args.batch:
@@ -889,7 +974,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(list(wl.CONFIGS) + list(wl.PAGED_CONFIGS) +
-                                   list(wl.FILL_CONFIGS)))
+                                   list(wl.FILL_CONFIGS) + list(wl.TOPK_CONFIGS)))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--max-rounds", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0,

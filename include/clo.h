@@ -195,6 +195,29 @@ clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int
                                  const clo_attn_opts* opts, cudaStream_t stream);
 
 /*
+ * clo_topk_retrieve -- top-k retrieval by exact qk-score (CLO section 2,
+ * Eq. 6: the ranking of keys by q . k does not depend on |q|; the decode
+ * flow's top-k retrieval stage, which the page runs with HATA hashing and no
+ * stated algorithm, so the exact ranking is computed).  For each batch row b
+ * and KV head g:
+ *     score(t) = (sum of the group's query vectors q_h) . K_t   (fp32)
+ * and idx[b][g] receives the k tokens with the largest score, equal scores at
+ * the cut going to the lower token, in ascending token order.
+ * q:         [B][Hq][d] fp16 (device).     K: [B][Hkv][T][d] fp16 (device).
+ * idx:       [B][Hkv][k] int32 output (device), e.g. the Cache Buffer index of
+ *            a token-addressed buffer.
+ * workspace: >= clo_topk_workspace_size(B, Hkv, T) bytes, 16-byte aligned
+ *            (the scores).
+ * opts:      optional; the events bracket the scoring kernel.
+ * Requires 0 <= k <= T, d == 128, G <= 8, B*Hkv <= 65535.
+ */
+size_t clo_topk_workspace_size(int B, int Hkv, int T);
+clo_status clo_topk_retrieve(const clo_half* q, const clo_half* K, int B, int Hq, int Hkv,
+                             int T, int d, int k, int32_t* idx, void* workspace,
+                             size_t ws_bytes, const clo_attn_opts* opts,
+                             cudaStream_t stream);
+
+/*
  * Workspace bytes clo_hybrid_decode_attn needs for these sizes when run with
  * num_ctas CTAs (0 = the default grid on the current device).  Returns 0 for
  * invalid sizes.  The workspace holds split-KV partial results; it needs no

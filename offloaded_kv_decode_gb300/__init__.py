@@ -58,6 +58,8 @@ _SIGS = {
                                _P], _I),
     "clo_plan_persistent": ([_P, _P, _I, _I, _F, ctypes.c_double, ctypes.c_double,
                              ctypes.c_double, _P, _P, _P, _P], _I),
+    "clo_topk_workspace_size": ([_I, _I, _I], _SZ),
+    "clo_topk_retrieve": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P], _I),
     "clo_hybrid_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_hybrid_decode_attn": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _F, _P, _P, _P, _SZ, _P, _P, _P], _I),
@@ -229,6 +231,31 @@ def clo_plan_persistent(tau, s_hat, eps: float, t_comp_s: float, link_bytes_per_
                                      D.ctypes.data, n_p.ctypes.data, n_persist.ctypes.data,
                                      ids.ctypes.data), "clo_plan_persistent")
     return dict(D=D, n_p=int(n_p[0]), n_persist=n_persist[:L].copy(), persist_ids=ids[:L].copy())
+
+
+# ---------------------------------------------------------------- top-k retrieval
+
+def clo_topk_workspace_size(B: int, Hkv: int, T: int) -> int:
+    return int(lib().clo_topk_workspace_size(B, Hkv, T))
+
+
+def clo_topk_retrieve(q: torch.Tensor, K: torch.Tensor, k: int, idx: torch.Tensor,
+                      workspace: torch.Tensor, num_ctas: int = 0, events=None, stream=None):
+    """Per KV head, the k keys with the largest (sum of the group's queries) . K_t,
+    ties to the lower token, ascending: q [B][Hq][d], K [B][Hkv][T][d] fp16,
+    idx [B][Hkv][k] int32 output."""
+    pq = _dev(q, "q", torch.float16, 3)
+    pk = _dev(K, "K", torch.float16, 4)
+    pi = _dev(idx, "idx", torch.int32, 3)
+    pw = _dev(workspace, "workspace", torch.uint8)
+    B, Hq, d = q.shape
+    Hkv, T = K.shape[1], K.shape[2]
+    if K.shape[0] != B or K.shape[3] != d or tuple(idx.shape) != (B, Hkv, k):
+        raise CloError("top-k shapes do not match", CLO_ERR_INVALID_ARG)
+    opts = _opts(num_ctas, events)
+    _check(lib().clo_topk_retrieve(pq, pk, B, Hq, Hkv, T, d, int(k), pi, pw, workspace.numel(),
+                                   ctypes.byref(opts) if opts is not None else None,
+                                   _stream(stream)), "clo_topk_retrieve")
 
 
 # ---------------------------------------------------------------- miss-path fill

@@ -1,0 +1,291 @@
+// clo_topk.cu -- top-k retrieval by exact qk-score (CLO section 2, Eq. 6: the
+// ranking of the keys by q . k does not depend on |q|; the decode flow's
+// top-k retrieval stage), for sm_103a.
+//
+// Per KV head g of batch row b, the score of key t is (sum of the group's G
+// query vectors) . K_t, accumulated in fp32; the k largest are selected, equal
+// scores at the cut going to the lower token index, and written in ascending
+// token order (so the output is deterministic).
+//
+// Two kernels:
+//   topk_score_kernel   streams every key once (HBM-bound: T * 256 bytes a
+//                       head).  A CTA owns a chunk of one head's keys; each
+//                       half-warp scores one 256-byte key row per step (16
+//                       bytes a lane, a 16-lane shuffle reduction), with 8
+//                       rows in flight per half-warp.
+//   topk_select_kernel  one CTA per head: a 4-pass radix select over the
+//                       order-preserving integer image of the fp32 scores
+//                       (8 bits a pass, shared-memory histogram) finds the
+//                       k-th largest key and how many of its ties to keep;
+//                       a last pass walks the tokens in order and writes the
+//                       selected ones with block-wide ballot prefix sums.
+#include <algorithm>
+
+#include "clo_device.cuh"
+
+namespace clo {
+
+constexpr int TK_D = 128;
+constexpr int TK_SCORE_THREADS = 256;
+constexpr int TK_UNROLL = 8;                                      // rows in flight a half-warp
+constexpr int TK_ROWS_PER_STEP = (TK_SCORE_THREADS / 16) * TK_UNROLL;  // 128 rows a CTA step
+constexpr int TK_SEL_THREADS = 1024;
+constexpr int TK_SEL_CACHE = 47 * 1024;  // keys of a row kept in shared memory (188 KB)
+constexpr int TK_MAX_G = 8;
+
+__global__ void __launch_bounds__(TK_SCORE_THREADS)
+    topk_score_kernel(const clo_half* __restrict__ q, const clo_half* __restrict__ K, int Hq,
+                      int Hkv, int G, int T, int chunk, float* __restrict__ scores) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int head = blockIdx.y;  // b * Hkv + g
+    const int b = head / Hkv, g = head - b * Hkv;
+    const int lane = threadIdx.x & 31, c = lane & 15, half = lane >> 4;
+    const int warp = threadIdx.x >> 5;
+    // Lane c holds dims [8c, 8c + 8) of the group's summed query.
+    float qs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qs[i] = 0.f;
+    const clo_half* qg = q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * TK_D + c * 8;
+    for (int j = 0; j < G; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qg + static_cast<size_t>(j) * TK_D);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            qs[2 * i] += f.x;
+            qs[2 * i + 1] += f.y;
+        }
+    }
+    const clo_half* Kh = K + static_cast<size_t>(head) * T * TK_D + c * 8;
+    float* sh = scores + static_cast<size_t>(head) * T;
+    const int t0 = blockIdx.x * chunk;
+    const int t1 = min(T, t0 + chunk);
+    // The loop runs on a warp-uniform base (the shuffles below need the whole
+    // warp); half-warp h of warp w takes rows base + h + 16 u.
+    for (int base = t0 + 2 * warp; base < t1; base += TK_ROWS_PER_STEP) {
+        uint4 kv[TK_UNROLL];
+#pragma unroll
+        for (int u = 0; u < TK_UNROLL; ++u) {
+            const int t = base + half + u * (TK_SCORE_THREADS / 16);
+            if (t < t1) kv[u] = *reinterpret_cast<const uint4*>(Kh + static_cast<size_t>(t) * TK_D);
+        }
+#pragma unroll
+        for (int u = 0; u < TK_UNROLL; ++u) {
+            const int t = base + half + u * (TK_SCORE_THREADS / 16);
+            float acc = 0.f;
+            if (t < t1) {
+                const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                    acc = fmaf(qs[2 * i], f.x, acc);
+                    acc = fmaf(qs[2 * i + 1], f.y, acc);
+                }
+            }
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, off);
+            if (c == 0 && t < t1) sh[t] = acc;
+        }
+    }
+}
+
+// Order-preserving image of an fp32 score (larger score, larger key; +0 and
+// -0 map to the same key).
+__device__ __forceinline__ uint32_t order_key(float s) {
+    uint32_t u = __float_as_uint(s == 0.f ? 0.f : s);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix of a per-thread 0/1 flag over the CTA (thread order) and
+// the CTA total: warp ballots, then warp 0 scans the per-warp counts.
+// wsum: TK_SEL_THREADS / 32 ints; woff: TK_SEL_THREADS / 32 + 1 ints.
+__device__ __forceinline__ int block_prefix(bool flag, int* wsum, int* woff, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned bal = __ballot_sync(FULL_MASK, flag);
+    if (lane == 0) wsum[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+        const int v = lane < TK_SEL_THREADS / 32 ? wsum[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(FULL_MASK, incl, off);
+            if (lane >= off) incl += u;
+        }
+        if (lane < TK_SEL_THREADS / 32) woff[lane] = incl - v;
+        if (lane == 31) woff[TK_SEL_THREADS / 32] = incl;
+    }
+    __syncthreads();
+    total = woff[TK_SEL_THREADS / 32];
+    return woff[warp] + __popc(bal & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(TK_SEL_THREADS)
+    topk_select_kernel(const float* __restrict__ scores, int T, int k, int32_t* __restrict__ idx) {
+    pdl_launch_dependents();
+    pdl_wait();
+    constexpr int kWarps = TK_SEL_THREADS / 32;
+    // One histogram per warp (no contention between warps); within a warp,
+    // lanes with the same digit are combined with a match before one add.
+    __shared__ int hist[kWarps][256];
+    __shared__ int total[256];
+    __shared__ int wsum[kWarps];
+    __shared__ int woff[kWarps + 1];
+    __shared__ uint32_t sel_prefix;
+    __shared__ int sel_need;
+    extern __shared__ uint32_t keys_sm[];  // the first min(T, TK_SEL_CACHE) keys
+    const int row = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float* s = scores + static_cast<size_t>(row) * T;
+    const int ncache = min(T, TK_SEL_CACHE);
+    // The row is read from L2 once, 8 loads in flight a thread; the passes
+    // below read shared memory (keys past the cache come from L2 each pass).
+    for (int t0 = threadIdx.x; t0 < ncache; t0 += 8 * TK_SEL_THREADS) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = t0 + u * TK_SEL_THREADS;
+            v[u] = t < ncache ? s[t] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = t0 + u * TK_SEL_THREADS;
+            if (t < ncache) keys_sm[t] = order_key(v[u]);
+        }
+    }
+    const auto key_at = [&](int t) { return t < ncache ? keys_sm[t] : order_key(s[t]); };
+    if (threadIdx.x == 0) {
+        sel_prefix = 0u;
+        sel_need = k;
+    }
+    uint32_t mask = 0u;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = lane; i < 256; i += 32) hist[warp][i] = 0;
+        __syncthreads();
+        const uint32_t prefix = sel_prefix;
+        // Warp-uniform trip count so every lane takes part in the match.
+        for (int t0 = warp * 32; t0 < T; t0 += TK_SEL_THREADS) {
+            const int t = t0 + lane;
+            int bin = 256;  // no key
+            if (t < T) {
+                const uint32_t key = key_at(t);
+                if ((key & mask) == prefix) bin = static_cast<int>((key >> shift) & 255u);
+            }
+            const unsigned same = __match_any_sync(FULL_MASK, bin);
+            if (bin < 256 && lane == __ffs(same) - 1) hist[warp][bin] += __popc(same);
+            __syncwarp();
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < 256; i += TK_SEL_THREADS) {
+            int n = 0;
+            for (int w = 0; w < kWarps; ++w) n += hist[w][i];
+            total[i] = n;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // Lane l owns digits 255 - 8l - 7 .. 255 - 8l (from the top): find
+            // the digit where the count from the top first reaches need.
+            const int need = sel_need;
+            int own = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) own += total[255 - 8 * lane - j];
+            int incl = own;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(FULL_MASK, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const unsigned reach = __ballot_sync(FULL_MASK, incl >= need);
+            const int l = __ffs(reach) - 1;  // need <= the bucket's count, so some lane reaches it
+            if (lane == l) {
+                int cum = incl - own;
+                int digit = 255 - 8 * l;
+                for (int j = 0; j < 8; ++j) {
+                    const int dgt = 255 - 8 * l - j;
+                    if (cum + total[dgt] >= need) {
+                        digit = dgt;
+                        break;
+                    }
+                    cum += total[dgt];
+                }
+                sel_need = need - cum;
+                sel_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
+            }
+        }
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    // kth = the k-th largest key; keep every larger key and the first `ties`
+    // keys equal to it, in token order.
+    const uint32_t kth = sel_prefix;
+    const int ties = sel_need;
+    int32_t* out = idx + static_cast<size_t>(row) * k;
+    int taken = 0, ties_seen = 0;
+    for (int t0 = 0; t0 < T; t0 += TK_SEL_THREADS) {
+        const int t = t0 + threadIdx.x;
+        const uint32_t key = t < T ? key_at(t) : 0u;
+        const bool tie = t < T && key == kth;
+        int tie_total;
+        const int tie_rank = ties_seen + block_prefix(tie, wsum, woff, tie_total);
+        const bool sel = t < T && (key > kth || (tie && tie_rank < ties));
+        int sel_total;
+        const int pos = taken + block_prefix(sel, wsum, woff, sel_total);
+        if (sel && pos < k) out[pos] = t;  // exactly k are selected; the test guards the store
+        taken += sel_total;
+        ties_seen += tie_total;
+    }
+}
+
+}  // namespace clo
+
+using namespace clo;
+
+extern "C" size_t clo_topk_workspace_size(int B, int Hkv, int T) {
+    if (B < 0 || Hkv <= 0 || T < 0) return 0;
+    return static_cast<size_t>(B) * Hkv * T * sizeof(float);
+}
+
+extern "C" clo_status clo_topk_retrieve(const clo_half* q, const clo_half* K, int B, int Hq,
+                                        int Hkv, int T, int d, int k, int32_t* idx,
+                                        void* workspace, size_t ws_bytes,
+                                        const clo_attn_opts* opts, cudaStream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T < 0 || k < 0 || k > T)
+        return CLO_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (d != TK_D || G > TK_MAX_G) return CLO_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Hkv > 65535 || T > (1 << 28)) return CLO_ERR_UNSUPPORTED;
+    if (B == 0 || k == 0) return CLO_OK;
+    if (q == nullptr || K == nullptr || idx == nullptr) return CLO_ERR_INVALID_ARG;
+    const auto aligned = [](const void* p, size_t a) {
+        return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+    };
+    if (!aligned(q, 16) || !aligned(K, 16) || !aligned(idx, 4)) return CLO_ERR_INVALID_ARG;
+    const size_t need = clo_topk_workspace_size(B, Hkv, T);
+    if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 16)) return CLO_ERR_WORKSPACE;
+    float* scores = static_cast<float*>(workspace);
+    const int heads = B * Hkv;
+    const int sms = device_sm_count();
+    if (sms <= 0) return CLO_ERR_CUDA;
+    // About 8 score CTAs per SM in total, each a multiple of one CTA step.
+    long long chunks = (static_cast<long long>(sms) * 8 + heads - 1) / heads;
+    long long chunk = (T + chunks - 1) / chunks;
+    chunk = std::max<long long>(TK_ROWS_PER_STEP, (chunk + TK_ROWS_PER_STEP - 1) / TK_ROWS_PER_STEP * TK_ROWS_PER_STEP);
+    chunks = (T + chunk - 1) / chunk;
+    if (opts != nullptr && opts->ev_begin != nullptr && !record_event(opts->ev_begin, stream))
+        return CLO_ERR_CUDA;
+    if (launch_pdl(topk_score_kernel, dim3(static_cast<unsigned>(chunks), heads),
+                   dim3(TK_SCORE_THREADS), 0, stream, q, K, Hq, Hkv, G, T,
+                   static_cast<int>(chunk), scores) != cudaSuccess)
+        return CLO_ERR_CUDA;
+    if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
+        return CLO_ERR_CUDA;
+    const size_t sel_smem = static_cast<size_t>(std::min(T, TK_SEL_CACHE)) * sizeof(uint32_t);
+    if (!prepare_kernel(reinterpret_cast<const void*>(topk_select_kernel),
+                        static_cast<int>(TK_SEL_CACHE * sizeof(uint32_t))))
+        return CLO_ERR_CUDA;
+    if (launch_pdl(topk_select_kernel, dim3(heads), dim3(TK_SEL_THREADS), sel_smem, stream,
+                   static_cast<const float*>(scores), T, k, idx) != cudaSuccess)
+        return CLO_ERR_CUDA;
+    return CLO_OK;
+}

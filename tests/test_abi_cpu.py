@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 14, names
+    assert len(names) == 16, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -157,3 +157,17 @@ def test_fused_lookup_rejects(L):
     assert fused(miss_count=None) == clo.CLO_ERR_INVALID_ARG
     assert fused(Hq=30) == clo.CLO_ERR_INVALID_ARG
     assert fused(B=9000) == clo.CLO_ERR_UNSUPPORTED
+
+
+def test_topk_rejects(L):
+    def topk(q=FAKE, K=FAKE, B=1, Hq=32, Hkv=8, T=100, d=128, k=10, ws=FAKE, wsb=1 << 30):
+        return L.clo_topk_retrieve(q, K, B, Hq, Hkv, T, d, k, FAKE, ws, wsb, None, None)
+    assert topk(k=101) == clo.CLO_ERR_INVALID_ARG        # k > T
+    assert topk(q=None) == clo.CLO_ERR_INVALID_ARG
+    assert topk(K=FAKE + 2) == clo.CLO_ERR_INVALID_ARG   # misaligned rows
+    assert topk(Hq=30) == clo.CLO_ERR_INVALID_ARG
+    assert topk(d=64) == clo.CLO_ERR_UNSUPPORTED
+    assert topk(Hq=72) == clo.CLO_ERR_UNSUPPORTED         # G = 9
+    assert topk(wsb=10) == clo.CLO_ERR_WORKSPACE
+    assert topk(k=0) == clo.CLO_OK and topk(B=0) == clo.CLO_OK
+    assert clo.clo_topk_workspace_size(2, 8, 100) == 2 * 8 * 100 * 4

@@ -127,6 +127,13 @@ FILL_CONFIGS = {
 }
 
 
+# Top-k retrieval: every KV head of the Llama3-8B-shaped batch-8 layer ranks
+# all of its 32768 keys against its query group and keeps the top 10%.
+TOPK_CONFIGS = {
+    "topk_llama3_8b_b8_32k": "llama3_8b_layer_b8_32k",
+}
+
+
 def small_hybrid(name="small", **kw) -> HybridConfig:
     """A reduced workload for quick parity runs (any field overridable)."""
     base = dict(B=2, L=1, Hq=32, Hkv=8, T=1000, Np=2, qmode="mix",
