@@ -97,28 +97,33 @@ __device__ __forceinline__ uint32_t order_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive prefix of a per-thread 0/1 flag over the CTA (thread order) and
-// the CTA total: warp ballots, then warp 0 scans the per-warp counts.
+// Exclusive prefix sum of a per-thread count over the CTA (thread order) and
+// the CTA total: a warp scan, then warp 0 scans the warp totals.
 // wsum: TK_SEL_THREADS / 32 ints; woff: TK_SEL_THREADS / 32 + 1 ints.
-__device__ __forceinline__ int block_prefix(bool flag, int* wsum, int* woff, int& total) {
+__device__ __forceinline__ int block_scan(int v, int* wsum, int* woff, int& total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(FULL_MASK, flag);
-    if (lane == 0) wsum[warp] = __popc(bal);
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(FULL_MASK, incl, off);
+        if (lane >= off) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int v = lane < TK_SEL_THREADS / 32 ? wsum[lane] : 0;
-        int incl = v;
+        const int w = lane < TK_SEL_THREADS / 32 ? wsum[lane] : 0;
+        int wi = w;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(FULL_MASK, incl, off);
-            if (lane >= off) incl += u;
+            const int u = __shfl_up_sync(FULL_MASK, wi, off);
+            if (lane >= off) wi += u;
         }
-        if (lane < TK_SEL_THREADS / 32) woff[lane] = incl - v;
-        if (lane == 31) woff[TK_SEL_THREADS / 32] = incl;
+        if (lane < TK_SEL_THREADS / 32) woff[lane] = wi - w;
+        if (lane == 31) woff[TK_SEL_THREADS / 32] = wi;
     }
     __syncthreads();
     total = woff[TK_SEL_THREADS / 32];
-    return woff[warp] + __popc(bal & ((1u << lane) - 1u));
+    return woff[warp] + incl - v;
 }
 
 __global__ void __launch_bounds__(TK_SEL_THREADS)
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
     __shared__ int wsum[kWarps];
     __shared__ int woff[kWarps + 1];
     __shared__ uint32_t sel_prefix;
-    __shared__ int sel_need;
+    __shared__ int sel_need, sel_equal;
     extern __shared__ uint32_t keys_sm[];  // the first min(T, TK_SEL_CACHE) keys
     const int row = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -164,17 +169,26 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
         for (int i = lane; i < 256; i += 32) hist[warp][i] = 0;
         __syncthreads();
         const uint32_t prefix = sel_prefix;
-        // Warp-uniform trip count so every lane takes part in the match.
-        for (int t0 = warp * 32; t0 < T; t0 += TK_SEL_THREADS) {
-            const int t = t0 + lane;
-            int bin = 256;  // no key
-            if (t < T) {
-                const uint32_t key = key_at(t);
-                if ((key & mask) == prefix) bin = static_cast<int>((key >> shift) & 255u);
+        // Warp-uniform trip count so every lane takes part in the match;
+        // four keys a lane per trip, and the adds are shared-memory atomics
+        // (nothing waits on them).
+        for (int t0 = warp * 32; t0 < T; t0 += 4 * TK_SEL_THREADS) {
+            int bin[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = t0 + u * TK_SEL_THREADS + lane;
+                bin[u] = 256;  // no key
+                if (t < T) {
+                    const uint32_t key = key_at(t);
+                    if ((key & mask) == prefix) bin[u] = static_cast<int>((key >> shift) & 255u);
+                }
             }
-            const unsigned same = __match_any_sync(FULL_MASK, bin);
-            if (bin < 256 && lane == __ffs(same) - 1) hist[warp][bin] += __popc(same);
-            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const unsigned same = __match_any_sync(FULL_MASK, bin[u]);
+                if (bin[u] < 256 && lane == __ffs(same) - 1)
+                    atomicAdd(&hist[warp][bin[u]], __popc(same));
+            }
         }
         __syncthreads();
         for (int i = threadIdx.x; i < 256; i += TK_SEL_THREADS) {
@@ -210,6 +224,7 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
                     cum += total[dgt];
                 }
                 sel_need = need - cum;
+                sel_equal = total[digit];  // after the last pass: the keys equal to the k-th
                 sel_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
             }
         }
@@ -217,23 +232,50 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
         __syncthreads();
     }
     // kth = the k-th largest key; keep every larger key and the first `ties`
-    // keys equal to it, in token order.
+    // keys equal to it, in token order.  Thread i takes keys 4i .. 4i + 3 of
+    // each 4096-key chunk, so thread order is token order.
     const uint32_t kth = sel_prefix;
     const int ties = sel_need;
+    const bool all_ties = ties == sel_equal;  // the usual case: no tie rank needed
     int32_t* out = idx + static_cast<size_t>(row) * k;
     int taken = 0, ties_seen = 0;
-    for (int t0 = 0; t0 < T; t0 += TK_SEL_THREADS) {
-        const int t = t0 + threadIdx.x;
-        const uint32_t key = t < T ? key_at(t) : 0u;
-        const bool tie = t < T && key == kth;
-        int tie_total;
-        const int tie_rank = ties_seen + block_prefix(tie, wsum, woff, tie_total);
-        const bool sel = t < T && (key > kth || (tie && tie_rank < ties));
+    for (int t0 = 0; t0 < T; t0 += 4 * TK_SEL_THREADS) {
+        const int tb = t0 + 4 * threadIdx.x;
+        uint32_t key[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) key[u] = tb + u < T ? key_at(tb + u) : 0u;
+        bool sel[4];
+        if (all_ties) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sel[u] = tb + u < T && key[u] >= kth;
+        } else {
+            int nt = 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) nt += (tb + u < T && key[u] == kth) ? 1 : 0;
+            int tie_total;
+            int rank = ties_seen + block_scan(nt, wsum, woff, tie_total);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = tb + u < T;
+                const bool tie = in && key[u] == kth;
+                sel[u] = in && (key[u] > kth || (tie && rank < ties));
+                rank += tie ? 1 : 0;
+            }
+            ties_seen += tie_total;
+        }
+        int ns = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ns += sel[u] ? 1 : 0;
         int sel_total;
-        const int pos = taken + block_prefix(sel, wsum, woff, sel_total);
-        if (sel && pos < k) out[pos] = t;  // exactly k are selected; the test guards the store
+        int pos = taken + block_scan(ns, wsum, woff, sel_total);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (sel[u]) {
+                if (pos < k) out[pos] = tb + u;  // exactly k are selected; the test guards the store
+                ++pos;
+            }
+        }
         taken += sel_total;
-        ties_seen += tie_total;
     }
 }
 
