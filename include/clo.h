@@ -209,7 +209,7 @@ clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int
  * workspace: >= clo_topk_workspace_size(B, Hkv, T) bytes, 16-byte aligned
  *            (the scores).
  * opts:      optional; the events bracket the scoring kernel.
- * Requires 0 <= k <= T, d == 128, G <= 8, B*Hkv <= 65535.
+ * Requires 0 <= k <= T <= 385024, d == 128, G <= 8, B*Hkv <= 65535.
  */
 size_t clo_topk_workspace_size(int B, int Hkv, int T);
 clo_status clo_topk_retrieve(const clo_half* q, const clo_half* K, int B, int Hq, int Hkv,

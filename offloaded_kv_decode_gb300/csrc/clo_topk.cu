@@ -13,13 +13,19 @@
 //                       half-warp scores one 256-byte key row per step (16
 //                       bytes a lane, a 16-lane shuffle reduction), with 8
 //                       rows in flight per half-warp.
-//   topk_select_kernel  one CTA per head: a 4-pass radix select over the
-//                       order-preserving integer image of the fp32 scores
-//                       (8 bits a pass, shared-memory histogram) finds the
-//                       k-th largest key and how many of its ties to keep;
-//                       a last pass walks the tokens in order and writes the
-//                       selected ones with block-wide ballot prefix sums.
+//   topk_select_kernel  one thread-block cluster per head, each CTA holding a
+//                       slice of the head's keys (the order-preserving
+//                       integer image of the fp32 scores) in shared memory:
+//                       a 4-pass radix select (8 bits a pass, per-warp
+//                       histograms summed over the cluster through
+//                       distributed shared memory) finds the k-th largest key
+//                       and how many of its ties to keep; a last pass walks
+//                       each slice in token order and writes the selected
+//                       tokens with block-wide prefix sums, offset by the
+//                       counts of the lower slices.
 #include <algorithm>
+
+#include <cooperative_groups.h>
 
 #include "clo_device.cuh"
 
@@ -30,7 +36,9 @@ constexpr int TK_SCORE_THREADS = 256;
 constexpr int TK_UNROLL = 8;                                      // rows in flight a half-warp
 constexpr int TK_ROWS_PER_STEP = (TK_SCORE_THREADS / 16) * TK_UNROLL;  // 128 rows a CTA step
 constexpr int TK_SEL_THREADS = 1024;
-constexpr int TK_SEL_CACHE = 47 * 1024;  // keys of a row kept in shared memory (188 KB)
+constexpr int TK_SEL_CACHE = 47 * 1024;  // keys a select CTA keeps in shared memory (188 KB)
+constexpr int TK_SEL_SLICE = 8 * 1024;   // aim for about this many keys a select CTA
+constexpr int TK_SEL_MAX_CLUSTER = 8;    // portable cluster size
 constexpr int TK_MAX_G = 8;
 
 __global__ void __launch_bounds__(TK_SCORE_THREADS)
@@ -126,75 +134,81 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* woff, int& tota
     return woff[warp] + incl - v;
 }
 
+// One cluster of `cs` CTAs per head (cs = gridDim.x / heads); CTA r of the
+// cluster caches keys [r * slice, (r + 1) * slice) in shared memory and every
+// pass sums the cluster's histograms through distributed shared memory, so
+// every CTA takes the same digit decisions.
 __global__ void __launch_bounds__(TK_SEL_THREADS)
-    topk_select_kernel(const float* __restrict__ scores, int T, int k, int32_t* __restrict__ idx) {
+    topk_select_kernel(const float* __restrict__ scores, int T, int k, int slice,
+                       int32_t* __restrict__ idx) {
+    namespace cg = cooperative_groups;
     pdl_launch_dependents();
     pdl_wait();
     constexpr int kWarps = TK_SEL_THREADS / 32;
-    // One histogram per warp (no contention between warps); within a warp,
-    // lanes with the same digit are combined with a match before one add.
-    __shared__ int hist[kWarps][256];
-    __shared__ int total[256];
+    __shared__ int hist[kWarps][256];  // one histogram per warp (no contention between warps)
+    __shared__ int total[256];         // this CTA's counts, read by the whole cluster
+    __shared__ int gtotal[256];
     __shared__ int wsum[kWarps];
     __shared__ int woff[kWarps + 1];
+    __shared__ int counts[2];          // this CTA's keys above and equal to the k-th
     __shared__ uint32_t sel_prefix;
-    __shared__ int sel_need, sel_equal;
-    extern __shared__ uint32_t keys_sm[];  // the first min(T, TK_SEL_CACHE) keys
-    const int row = blockIdx.x;
+    __shared__ int sel_need;
+    extern __shared__ uint32_t keys_sm[];  // this CTA's slice of the row
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cs = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int row = blockIdx.x / cs;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float* s = scores + static_cast<size_t>(row) * T;
-    const int ncache = min(T, TK_SEL_CACHE);
-    // The row is read from L2 once, 8 loads in flight a thread; the passes
-    // below read shared memory (keys past the cache come from L2 each pass).
-    for (int t0 = threadIdx.x; t0 < ncache; t0 += 8 * TK_SEL_THREADS) {
+    const int lo = min(T, rank * slice), hi = min(T, lo + slice), n = hi - lo;
+    const float* s = scores + static_cast<size_t>(row) * T + lo;
+    // The slice is read from L2 once, 8 loads in flight a thread.
+    for (int t0 = threadIdx.x; t0 < n; t0 += 8 * TK_SEL_THREADS) {
         float v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int t = t0 + u * TK_SEL_THREADS;
-            v[u] = t < ncache ? s[t] : 0.f;
+            v[u] = t < n ? s[t] : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int t = t0 + u * TK_SEL_THREADS;
-            if (t < ncache) keys_sm[t] = order_key(v[u]);
+            if (t < n) keys_sm[t] = order_key(v[u]);
         }
     }
-    const auto key_at = [&](int t) { return t < ncache ? keys_sm[t] : order_key(s[t]); };
     if (threadIdx.x == 0) {
         sel_prefix = 0u;
         sel_need = k;
     }
     uint32_t mask = 0u;
+    int last_digit = 0;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = lane; i < 256; i += 32) hist[warp][i] = 0;
         __syncthreads();
         const uint32_t prefix = sel_prefix;
-        // Warp-uniform trip count so every lane takes part in the match;
-        // four keys a lane per trip, and the adds are shared-memory atomics
-        // (nothing waits on them).
-        for (int t0 = warp * 32; t0 < T; t0 += 4 * TK_SEL_THREADS) {
-            int bin[4];
+        // Four keys a lane per trip; the adds are shared-memory atomics on
+        // the warp's own histogram (nothing waits on them, and lanes that hit
+        // the same bin are resolved by the atomic unit).
+        for (int t0 = warp * 32; t0 < n; t0 += 4 * TK_SEL_THREADS) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int t = t0 + u * TK_SEL_THREADS + lane;
-                bin[u] = 256;  // no key
-                if (t < T) {
-                    const uint32_t key = key_at(t);
-                    if ((key & mask) == prefix) bin[u] = static_cast<int>((key >> shift) & 255u);
+                if (t < n) {
+                    const uint32_t key = keys_sm[t];
+                    if ((key & mask) == prefix) atomicAdd(&hist[warp][(key >> shift) & 255u], 1);
                 }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const unsigned same = __match_any_sync(FULL_MASK, bin[u]);
-                if (bin[u] < 256 && lane == __ffs(same) - 1)
-                    atomicAdd(&hist[warp][bin[u]], __popc(same));
             }
         }
         __syncthreads();
         for (int i = threadIdx.x; i < 256; i += TK_SEL_THREADS) {
-            int n = 0;
-            for (int w = 0; w < kWarps; ++w) n += hist[w][i];
-            total[i] = n;
+            int c = 0;
+            for (int w = 0; w < kWarps; ++w) c += hist[w][i];
+            total[i] = c;
+        }
+        cluster.sync();  // every CTA's counts are final
+        for (int i = threadIdx.x; i < 256; i += TK_SEL_THREADS) {
+            int c = 0;
+            for (int r = 0; r < cs; ++r) c += cluster.map_shared_rank(total, r)[i];
+            gtotal[i] = c;
         }
         __syncthreads();
         if (warp == 0) {
@@ -203,7 +217,7 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
             const int need = sel_need;
             int own = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) own += total[255 - 8 * lane - j];
+            for (int j = 0; j < 8; ++j) own += gtotal[255 - 8 * lane - j];
             int incl = own;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -217,49 +231,71 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
                 int digit = 255 - 8 * l;
                 for (int j = 0; j < 8; ++j) {
                     const int dgt = 255 - 8 * l - j;
-                    if (cum + total[dgt] >= need) {
+                    if (cum + gtotal[dgt] >= need) {
                         digit = dgt;
                         break;
                     }
-                    cum += total[dgt];
+                    cum += gtotal[dgt];
                 }
                 sel_need = need - cum;
-                sel_equal = total[digit];  // after the last pass: the keys equal to the k-th
                 sel_prefix = prefix | (static_cast<uint32_t>(digit) << shift);
             }
         }
         mask |= 255u << shift;
         __syncthreads();
+        last_digit = static_cast<int>((sel_prefix >> shift) & 255u);
+        cluster.sync();  // nobody reads this pass's counts any more
     }
-    // kth = the k-th largest key; keep every larger key and the first `ties`
-    // keys equal to it, in token order.  Thread i takes keys 4i .. 4i + 3 of
-    // each 4096-key chunk, so thread order is token order.
+    // kth = the k-th largest key of the row; the row keeps every larger key
+    // and the first `ties` keys equal to it, in token order.
     const uint32_t kth = sel_prefix;
     const int ties = sel_need;
-    const bool all_ties = ties == sel_equal;  // the usual case: no tie rank needed
+    // This CTA's keys above the k-th and equal to it.
+    int above = 0;
+    for (int t = threadIdx.x; t < n; t += TK_SEL_THREADS) above += keys_sm[t] > kth ? 1 : 0;
+    int above_total;
+    (void)block_scan(above, wsum, woff, above_total);
+    if (threadIdx.x == 0) {
+        counts[0] = above_total;
+        counts[1] = total[last_digit];  // the last pass counted exactly the keys equal to kth
+    }
+    cluster.sync();
+    int out_base = 0, ties_before = 0;
+    for (int r = 0; r < rank; ++r) {
+        const int* c = cluster.map_shared_rank(counts, r);
+        const int eq = c[1];
+        const int take = min(eq, max(ties - ties_before, 0));
+        out_base += c[0] + take;
+        ties_before += eq;
+    }
+    cluster.sync();  // the other CTAs' counts are no longer read
+    const int my_ties = min(counts[1], max(ties - ties_before, 0));
+    const bool all_ties = my_ties == counts[1];  // the usual case: no tie rank needed
+    // Thread i takes keys 4i .. 4i + 3 of each 4096-key chunk, so thread
+    // order is token order.
     int32_t* out = idx + static_cast<size_t>(row) * k;
-    int taken = 0, ties_seen = 0;
-    for (int t0 = 0; t0 < T; t0 += 4 * TK_SEL_THREADS) {
+    int taken = out_base, ties_seen = 0;
+    for (int t0 = 0; t0 < n; t0 += 4 * TK_SEL_THREADS) {
         const int tb = t0 + 4 * threadIdx.x;
         uint32_t key[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) key[u] = tb + u < T ? key_at(tb + u) : 0u;
+        for (int u = 0; u < 4; ++u) key[u] = tb + u < n ? keys_sm[tb + u] : 0u;
         bool sel[4];
         if (all_ties) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) sel[u] = tb + u < T && key[u] >= kth;
+            for (int u = 0; u < 4; ++u) sel[u] = tb + u < n && key[u] >= kth;
         } else {
             int nt = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) nt += (tb + u < T && key[u] == kth) ? 1 : 0;
+            for (int u = 0; u < 4; ++u) nt += (tb + u < n && key[u] == kth) ? 1 : 0;
             int tie_total;
-            int rank = ties_seen + block_scan(nt, wsum, woff, tie_total);
+            int rnk = ties_seen + block_scan(nt, wsum, woff, tie_total);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const bool in = tb + u < T;
+                const bool in = tb + u < n;
                 const bool tie = in && key[u] == kth;
-                sel[u] = in && (key[u] > kth || (tie && rank < ties));
-                rank += tie ? 1 : 0;
+                sel[u] = in && (key[u] > kth || (tie && rnk < my_ties));
+                rnk += tie ? 1 : 0;
             }
             ties_seen += tie_total;
         }
@@ -271,7 +307,7 @@ __global__ void __launch_bounds__(TK_SEL_THREADS)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             if (sel[u]) {
-                if (pos < k) out[pos] = tb + u;  // exactly k are selected; the test guards the store
+                if (pos < k) out[pos] = lo + tb + u;  // exactly k are selected; the test guards the store
                 ++pos;
             }
         }
@@ -296,7 +332,8 @@ extern "C" clo_status clo_topk_retrieve(const clo_half* q, const clo_half* K, in
         return CLO_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
     if (d != TK_D || G > TK_MAX_G) return CLO_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * Hkv > 65535 || T > (1 << 28)) return CLO_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Hkv > 65535 || T > TK_SEL_MAX_CLUSTER * TK_SEL_CACHE)
+        return CLO_ERR_UNSUPPORTED;
     if (B == 0 || k == 0) return CLO_OK;
     if (q == nullptr || K == nullptr || idx == nullptr) return CLO_ERR_INVALID_ARG;
     const auto aligned = [](const void* p, size_t a) {
@@ -322,12 +359,20 @@ extern "C" clo_status clo_topk_retrieve(const clo_half* q, const clo_half* K, in
         return CLO_ERR_CUDA;
     if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
-    const size_t sel_smem = static_cast<size_t>(std::min(T, TK_SEL_CACHE)) * sizeof(uint32_t);
+    // Cluster of cs CTAs per head, each caching a slice of at most
+    // TK_SEL_CACHE keys; at least 4 when the row is long enough, so one head's
+    // passes are spread over several SMs.
+    int cs = static_cast<int>((static_cast<long long>(T) + TK_SEL_SLICE - 1) / TK_SEL_SLICE);
+    cs = std::max(1, std::min(TK_SEL_MAX_CLUSTER, cs));
+    const int slice = (T + cs - 1) / cs;
+    if (slice > TK_SEL_CACHE) return CLO_ERR_UNSUPPORTED;
+    const size_t sel_smem = static_cast<size_t>(slice) * sizeof(uint32_t);
     if (!prepare_kernel(reinterpret_cast<const void*>(topk_select_kernel),
                         static_cast<int>(TK_SEL_CACHE * sizeof(uint32_t))))
         return CLO_ERR_CUDA;
-    if (launch_pdl(topk_select_kernel, dim3(heads), dim3(TK_SEL_THREADS), sel_smem, stream,
-                   static_cast<const float*>(scores), T, k, idx) != cudaSuccess)
+    if (launch_pdl_cluster(topk_select_kernel, dim3(heads * cs), dim3(TK_SEL_THREADS), sel_smem,
+                           stream, static_cast<unsigned>(cs), static_cast<const float*>(scores), T,
+                           k, slice, idx) != cudaSuccess)
         return CLO_ERR_CUDA;
     return CLO_OK;
 }
