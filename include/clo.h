@@ -13,10 +13,15 @@
  * attention over per-request KV).  The attention itself is
  * softmax(q K^T / sqrt(d_head)) V as written in "KVPR: Efficient LLM
  * Inference With I/O-Aware KV Cache Partial Recomputation", section A3.
+ * Around them: the miss-path fill that writes missed heads' top-k rows into
+ * the Cache Buffer (CLO section 3, Fig. 7), the offline persistent-head plan
+ * (CLO Eqs. 11-13), the next layer's lookup carried in an attention launch
+ * (CLO section 3, Fig. 9) and top-k retrieval by exact qk-score (CLO Eq. 6).
  *
  * Conventions shared by every entry point:
- *  - Tensor pointers are DEVICE pointers owned by the caller, row-major and
- *    contiguous in the layouts stated per call.  fp16 data is IEEE binary16
+ *  - Tensor pointers are DEVICE pointers owned by the caller (unless a call
+ *    states otherwise), row-major and contiguous in the layouts stated per
+ *    call.  fp16 data is IEEE binary16
  *    (clo_half holds the bit pattern).  The library never allocates or frees
  *    device memory; scratch space is caller-provided ("workspace").
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream) and
@@ -35,9 +40,10 @@
  *  - Query head h belongs to KV head h / G with G = Hq / Hkv (contiguous
  *    grouping).  d (head dimension) must be 128 in this build.
  *  - No C++ exception crosses this interface.  There is no global mutable
- *    state besides cached device attributes, so independent calls on
- *    different streams may run concurrently provided they do not share
- *    output or workspace buffers.
+ *    state besides cached device attributes (and the fixed scratch of
+ *    clo_hybrid_decode_attn_noalloc), so independent calls on different
+ *    streams may run concurrently provided they do not share output or
+ *    workspace buffers.
  */
 #ifndef CLO_H_
 #define CLO_H_
@@ -63,7 +69,8 @@ typedef enum clo_status {
 } clo_status;
 
 /* Bits a kernel ORs into *err_flag. */
-#define CLO_FLAG_BAD_INDEX 0x1   /* Cache Buffer index or block-table entry out of range */
+#define CLO_FLAG_BAD_INDEX 0x1   /* Cache Buffer index, block-table entry, or a fill's
+                                    miss-list entry, token or slot out of range */
 #define CLO_FLAG_BAD_PERSIST 0x2 /* persist_ids entry out of range or repeated */
 #define CLO_FLAG_BAD_CTX 0x4     /* a context length < 0 or > max_blocks*block_size */
 

@@ -13,7 +13,7 @@ extern "C" const char* clo_status_string(clo_status s) {
     return "CLO_ERR_UNKNOWN";
 }
 
-extern "C" int clo_version(void) { return 100; }
+extern "C" int clo_version(void) { return 10100; }  // 1.1.0
 
 extern "C" clo_status clo_check_error_flag(int32_t host_err_flag) {
     return host_err_flag == 0 ? CLO_OK : CLO_ERR_BAD_INDEX;

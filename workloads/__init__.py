@@ -51,6 +51,8 @@ class HybridConfig:
     addressing: str = "token"    # "token": C = T slots, idx = positions in [0, T)
                                  # "compact": C = k slots, idx = permutation of [0, k)
     ring: int = 0                # >0: only `ring` physical layer buffers, reused cyclically
+    idx_order: str = "random"    # "random": idx in random order; "sorted": ascending, as
+                                 # the top-k retrieval writes it
     seed: int = 1234
 
     @property
@@ -105,6 +107,11 @@ CONFIGS = {
         qmode="mix", smode="uniform", seed=1236),
     # Qwen2.5-14B-shaped decode step: 48 layers, GQA 5, batch 16, context 64K,
     # 15% of heads with cosine ~0.6; a ring of 8 physical layer buffers.
+    # The batch-8 layer with each head's Cache Buffer indices in ascending
+    # order (as the top-k retrieval writes them): measured beside the default.
+    "llama3_8b_layer_b8_32k_sorted": HybridConfig(
+        "llama3_8b_layer_b8_32k_sorted", B=8, L=1, Hq=32, Hkv=8, T=32768, Np=2,
+        qmode="cos", c_lo=0.7, c_hi=0.9, smode="beta", idx_order="sorted", seed=1235),
     "qwen25_14b_step_b16_64k": HybridConfig(
         "qwen25_14b_step_b16_64k", B=16, L=48, Hq=40, Hkv=8, T=65536, Np=1,
         qmode="cos", c_lo=0.7, c_hi=0.9, low_frac=0.15, smode="beta", ring=8,
@@ -233,6 +240,8 @@ def cache_buffer(cfg: HybridConfig, layer: int, device="cpu"):
     cbV = torch.randn(shape, generator=g, device=device, dtype=torch.float16)
     keys = torch.rand((cfg.B * cfg.Hkv, cfg.C), generator=g, device=device)
     idx = keys.argsort(dim=1)[:, : cfg.k].to(torch.int32)
+    if cfg.idx_order == "sorted":
+        idx = idx.sort(dim=1).values
     return cbK, cbV, idx.reshape(cfg.B, cfg.Hkv, cfg.k).contiguous()
 
 
