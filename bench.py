@@ -689,25 +689,34 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_digest(path: str) -> str:
+    """sha256 (first 16 hex digits) of a source file's code: comments removed
+    and whitespace collapsed, so only a change to the code itself changes it."""
+    import hashlib
+    import re
+
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"\s+", " ", src).strip()
+    return hashlib.sha256(src.encode()).hexdigest()[:16]
+
+
 def traffic_from_profiles(kernel_file: str, kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; else None."""
-    import hashlib
-
+    the current kernel code; else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         text = open(path).read()
     except OSError:
         return None
-    src = open(kernel_file, "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
     got, traffic = None, None
     for line in text.splitlines():
-        if line.startswith("source_sha256_16:"):
+        if line.startswith("code_sha256_16:"):
             got = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
-    return traffic if (got == sha and traffic is not None) else None
+    return traffic if (got == code_digest(kernel_file) and traffic is not None) else None
 
 
 def dist_setup(gpus: int):

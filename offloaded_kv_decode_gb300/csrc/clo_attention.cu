@@ -9,17 +9,22 @@
 //
 // Design (one GPU, HBM-bound):
 //  * Work unit: a 16-token tile of one "segment" (one batch row / request and
-//    one KV head).  All tiles of all segments form one flat stream, which is
-//    cut into C equal contiguous ranges, one per CTA (C = SM count).  Every SM
-//    therefore streams the same number of KV bytes whether a tile comes from a
-//    128K-token persistent head or from a 13K-row top-k head -- the few long
-//    persistent heads cannot serialise the launch.
-//  * Inside a CTA the 8 warps take the range's tiles round-robin.  Each warp
-//    keeps its own 3-stage shared-memory ring filled by 16-byte cp.async
-//    copies (K and V rows of a tile: 8 KB), so ~128 KB per SM is in flight.
+//    one KV head).  The tiles form one stream per part (hybrid: the
+//    contiguous Persistent Cache tiles, then the indexed Cache Buffer tiles;
+//    paged: one part), and every part is cut into C equal contiguous ranges,
+//    one per CTA (C = SMs x CTAs per SM, one wave).  Every CTA therefore
+//    streams the same mix of contiguous and scattered bytes whether a tile
+//    comes from a 128K-token persistent head or a 13K-row top-k head.  Odd
+//    CTAs take their two ranges in the opposite order, so the grid never
+//    switches from contiguous to scattered rows all at once.
+//  * Three CTAs of four warps share an SM; the warps take their CTA's tiles
+//    round-robin.  Each warp keeps a 2-stage shared-memory ring filled by
+//    16-byte cp.async copies with an L2 evict-first hint (K and V rows of a
+//    tile: 8 KB), one tile in flight while it computes the previous one.
 //    Rows are XOR-swizzled in 16-byte chunks so ldmatrix reads are bank-
 //    conflict free.  Indexed rows (Cache Buffer) and block-table rows cost the
-//    same as contiguous rows: every copy is a whole 256-byte row.
+//    same number of copies as contiguous rows: every copy is a whole
+//    256-byte row.
 //  * Math on the tensor cores with mma.sync m16n8k16 (fp16 in, fp32 accum):
 //    S = K_tile Q^T puts the 16 tokens on M and the G <= 8 query heads of the
 //    KV group on N (one n8 tile), then O^T += V_tile^T P^T puts the 128 head
@@ -29,9 +34,12 @@
 //  * Each CTA merges its warps' (m, l, O) in shared memory whenever its range
 //    crosses a segment end.  A segment that lies wholly in one CTA is written
 //    straight to the output; a segment cut by CTA boundaries leaves one fp32
-//    partial per CTA in the workspace (slot c + s, unique because both
-//    partitions are contiguous) and a second small kernel merges those
-//    partials by log-sum-exp.
+//    partial per CTA in the workspace (slot c + s + part * C, unique because
+//    both partitions are contiguous) and a second small kernel merges those
+//    partials by log-sum-exp.  That merge launch can also carry the next
+//    layer's lookup (clo_hybrid_decode_attn_lookup).
+//  * Every kernel uses programmatic dependent launch, so each grid becomes
+//    resident while its predecessor drains.
 //  * Bad indices, block-table entries, context lengths or persistent ids are
 //    never dereferenced: the copy is zero-filled, the row masked, an error bit
 //    is ORed into err_flag and the affected outputs are written as zeros.
