@@ -7,19 +7,24 @@ dense decode attention, through libclo.
                     [--impl ours|reference]
 
 One step = one decode step of the workload: the thresholds launch, then for
-every layer the fused lookup + label update and the hybrid attention (for the
-paged workload: one paged attention call).  Inputs are seeded synthetic
-tensors (workloads/), resident in HBM before timing.  Every workload cycles
-over physical buffer sets so that the bytes between two reads of the same
-address exceed the 129 MB L2 (no L2 flush is needed).
+every layer the hybrid attention with the next layer's fused lookup + label
+update carried in the same launches (--lookup-schedule picks the
+alternatives); for the paged workload one paged attention call; for the
+fill and top-k workloads one miss-path fill or one top-k retrieval of a
+layer.  Inputs are seeded synthetic tensors (workloads/), resident in device
+memory (the fill's full KV copy in pinned host memory for the host-link
+variant) before timing.  Every workload cycles over physical buffer sets so
+that the bytes between two reads of the same address exceed the 129 MB L2
+(no L2 flush is needed).
 
 The step is captured once per buffer phase as a CUDA graph and replayed; K
 steps are timed with CUDA events between a barrier + synchronize on both
 sides, repeated in rounds of exactly K steps until about a second of GPU time
 has been covered (so the clock sampler sees the load); the median round is
 reported.  A second copy of each graph with CUDA events around the main
-attention kernel is replayed after every timed round; those events give the
-kernel's duration for the roofline line.
+kernel (the attention's split kernel, the fill kernel or the top-k scoring
+kernel) is replayed after every timed round; those events give the kernel's
+duration for the roofline line.
 
 Multi-GPU (torchrun): every rank runs an independent replica on its own
 inputs (the path has no exchange step), value = bytes of all ranks / max time.
