@@ -1,10 +1,12 @@
 """Python binding of libclo (include/clo.h): argument marshalling only.
 
-Every function here checks the torch tensors it is given (device, dtype,
-contiguity, shapes), passes their device pointers and the CUDA stream to the
-C ABI of ``libclo.so`` and raises ``CloError`` on a non-OK status.  All
-computation happens in the library's CUDA kernels; there is no CPU path.  If
-the library has not been built, the first call raises ``CloError``.
+Every function here checks the tensors it is given (device, dtype,
+contiguity, shapes), passes their pointers and the CUDA stream to the C ABI of
+``libclo.so`` and raises ``CloError`` on a non-OK status.  All computation
+happens inside libclo: in its CUDA kernels, and for the offline
+persistent-head plan in the library's host code; there is no Python or torch
+fallback.  If the library has not been built, the first call raises
+``CloError``.
 
 Torch is used for device memory, streams and events only.
 """
