@@ -55,6 +55,7 @@ import workloads as wl  # noqa: E402
 METRIC = ("µs per layer-step and achieved HBM GB/s (% of GB300 peak) for lookup+attention")
 DEFAULT_WORKLOAD = "llama3_8b_layer_b8_32k"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 L2_BYTES = 129 * 2 ** 20
 HALF = 2
 
@@ -268,6 +269,23 @@ class HybridWorkload:
             self.h_sim[j].copy_(it["sim"], non_blocking=True)
             self.h_miss[j].copy_(it["miss"], non_blocking=True)
             self.h_nmiss[j].copy_(it["nmiss"], non_blocking=True)
+
+    def lookup_stats(self) -> dict:
+        """Hit rate and near-threshold count of the lookups' last results over
+        all buffer sets (read back after the timed region)."""
+        cfg = self.cfg
+        hits = misses = near = 0
+        for j, it in enumerate(self.inst):
+            flag = it["flag"].cpu().numpy()
+            sim = it["sim"].cpu().numpy().reshape(cfg.B, cfg.Hkv)
+            tau = self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv].cpu().numpy()
+            looked = flag != 2
+            hits += int(((flag == 0) & looked).sum())
+            misses += int(((flag == 1) & looked).sum())
+            near += int((np.abs(sim - tau[None, :]).ravel()[looked] < 1e-4).sum())
+        n = hits + misses
+        return {"hit_rate": hits / n if n else None, "looked_up_heads": n,
+                "near_tau_groups": near}
 
     def config(self) -> dict:
         c = self.cfg
@@ -720,7 +738,10 @@ def traffic_from_profiles(kernel_file: str, kernel: str, workload: str):
         if line.startswith("code_sha256_16:"):
             got = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
+            try:
+                traffic = float(line.split(":", 1)[1].split()[0])
+            except (IndexError, ValueError):
+                traffic = None
     return traffic if (got == code_digest(kernel_file) and traffic is not None) else None
 
 
@@ -936,6 +957,11 @@ def run_ours(args):
                    "graph_phases": W.phases},
         "clocks": clocks,
     }
+    line["peaks"] = {"measured_hbm_gbs": peak_hbm()[0], "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+                     "step_frac_of_nominal": value / world / NOMINAL_HBM_GBS}
+    if W.kind == "hybrid":
+        line["tokens_per_s"] = W.cfg.B * world / (ms_step * 1e-3)
+        line["lookup"] = W.lookup_stats()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:

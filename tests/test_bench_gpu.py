@@ -1,0 +1,38 @@
+"""bench.py end to end on small cases of every workload kind: the JSON line
+carries the contract's keys and sane values."""
+import contextlib
+import io
+import json
+
+import pytest
+
+import bench
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("args", [
+    ["--workload", "tiny"],
+    ["--workload", "tiny", "--lookup-schedule", "stream"],
+    ["--workload", "tiny", "--lookup-schedule", "serial"],
+    ["--workload", "paged_llama2_7b_b256", "--batch", "8"],
+    ["--workload", "fill_hbm_llama3_8b_b8_32k", "--batch", "1"],
+    ["--workload", "fill_c2c_llama3_8b_b8_32k", "--batch", "1"],
+    ["--workload", "topk_llama3_8b_b8_32k", "--batch", "1"],
+], ids=lambda a: "_".join(x.lstrip("-") for x in a[1::2] if x not in ("--batch",)))
+def test_bench_line(args):
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(args + ["--steps", "3", "--warmup", "3", "--max-rounds", "1",
+                           "--no-cpu-baseline"])
+    d = json.loads(buf.getvalue().strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "dtype", "data", "config", "roofline", "e2e",
+                "gpu_launches", "clocks"):
+        assert key in d, key
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["gpu_launches"] > 0
+    r = d["roofline"]
+    assert r["bound"] in ("hbm", "c2c") and r["achieved"] > 0 and r["peak"] > 0
+    assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
+    if "lookup" in d:
+        assert d["lookup"]["looked_up_heads"] > 0 and d["tokens_per_s"] > 0
