@@ -1045,9 +1045,8 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Records a timing event on the stream.  Under stream capture the record is
-// made external so it becomes an event node of the graph (re-recorded on
-// every replay) rather than an internal ordering edge.
+// Bytes of the split-KV partials: [slots][G][128] fp32 outputs, then
+// [slots][G] fp32 log2-sum-exps, each padded to 256 bytes.
 static size_t partial_bytes(long long slots, int G) {
     const size_t o = static_cast<size_t>(slots) * G * D * sizeof(float);
     const size_t l = static_cast<size_t>(slots) * G * sizeof(float);
