@@ -118,7 +118,7 @@ class HybridWorkload:
             s_np = wl.importance(cfg, li)
             s_all.append(s_np)
             self.inst.append(dict(
-                q=q, labels=lab, cbK=cbK, cbV=cbV, idx=idx, pK=pK, pV=pV,
+                q=q, labels=lab, labels0=lab.clone(), cbK=cbK, cbV=cbV, idx=idx, pK=pK, pV=pV,
                 pid=torch.from_numpy(wl.persist_ids(cfg, li)).to(dev),
                 pmask=torch.from_numpy(wl.persist_mask(cfg, li)).to(dev),
                 w=torch.from_numpy(s_np).to(dev),
@@ -270,12 +270,19 @@ class HybridWorkload:
             self.h_miss[j].copy_(it["miss"], non_blocking=True)
             self.h_nmiss[j].copy_(it["nmiss"], non_blocking=True)
 
-    def lookup_stats(self) -> dict:
-        """Hit rate and near-threshold count of the lookups' last results over
-        all buffer sets (read back after the timed region)."""
-        cfg = self.cfg
+    def lookup_stats(self, reps: int = 50) -> dict:
+        """The lookup on its own, after the timed region: hit rate and
+        near-threshold count of one lookup per buffer set against the
+        generator's labels (the timed steps overwrite the labels of missed
+        heads with the same queries, so later lookups of a set all hit), and
+        the standalone time of clo_lookup_update (CUDA events around a graph
+        of `reps` back-to-back calls on fresh label copies)."""
+        torch, clo, cfg = self.torch, self.clo, self.cfg
         hits = misses = near = 0
         for j, it in enumerate(self.inst):
+            lab = it["labels0"].clone()
+            clo.clo_lookup_update(it["q"], lab, it["w"], self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv],
+                                  it["pmask"], it["flag"], it["sim"], it["miss"], it["nmiss"])
             flag = it["flag"].cpu().numpy()
             sim = it["sim"].cpu().numpy().reshape(cfg.B, cfg.Hkv)
             tau = self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv].cpu().numpy()
@@ -284,8 +291,29 @@ class HybridWorkload:
             misses += int(((flag == 1) & looked).sum())
             near += int((np.abs(sim - tau[None, :]).ravel()[looked] < 1e-4).sum())
         n = hits + misses
+        labs = [it["labels0"].clone() for it in self.inst]
+
+        def calls():
+            for r in range(reps):
+                j = r % self.n_inst
+                it = self.inst[j]
+                clo.clo_lookup_update(it["q"], labs[j], it["w"],
+                                      self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv], it["pmask"],
+                                      it["flag"], it["sim"], it["miss"], it["nmiss"])
+
+        # Captured as one graph, so the host's launch rate does not set the time.
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            calls()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
         return {"hit_rate": hits / n if n else None, "looked_up_heads": n,
-                "near_tau_groups": near}
+                "near_tau_groups": near, "standalone_us_per_call": a.elapsed_time(b) * 1e3 / reps}
 
     def config(self) -> dict:
         c = self.cfg
