@@ -254,6 +254,20 @@ struct HybridGeo {
         return g;
     }
     __device__ bool all_bad(const int* sm) const { return sm[0] == 0; }
+    // Brings the Cache Buffer indices of tiles [t0, t0 + n) of part 1 into L2
+    // (the lines holding each tile's first and last index), so that the
+    // per-tile index loads, issued one pipeline step ahead of their copies,
+    // hit L2 instead of waiting on DRAM behind the K/V stream.  Needs the slot
+    // table (cta_init).
+    __device__ void prefetch_indices(const int* sm, long long t0, long long n) const {
+        for (long long i = threadIdx.x; i < n; i += blockDim.x) {
+            const Seg g = segment(seg_of(t0 + i, sm), sm);
+            const int tok = static_cast<int>(t0 + i - g.first) * TILE;
+            const int32_t* row = idx + (static_cast<long long>(g.b) * Hkv + g.kv) * k;
+            prefetch_l2(row + tok);
+            prefetch_l2(row + min(tok + TILE - 1, k - 1));
+        }
+    }
     // The indirection of row r (0..15) of a tile: its Cache Buffer index
     // (0 for persistent rows and rows past the end).  Issued one pipeline
     // step before the row is copied so its latency overlaps the math.
@@ -386,6 +400,7 @@ struct PagedGeo {
         return g;
     }
     __device__ bool all_bad(const int*) const { return false; }
+    __device__ void prefetch_indices(const int*, long long, long long) const {}
     // The block holding tile `tile_in` (the same for all 16 rows).
     __device__ int row_load(const Seg& g, int tile_in, int /*r*/) const {
         return __ldg(block_table + static_cast<long long>(g.b) * max_blocks + tile_in);
@@ -441,10 +456,11 @@ __device__ __forceinline__ void prefetch_tile(const Geo& geo, const int* gsm, lo
 
 // Issues the cp.async copies of one tile (16 K rows + 16 V rows) into a ring
 // stage and records its row masks (bits 0-15 valid rows, 16-31 bad rows).
+// dry: every copy is a zero-fill that reads no global memory.
 template <class Geo>
 __device__ __forceinline__ void issue_tile(const Geo& geo, const int* gsm, const Pending& pd,
                                            uint32_t stage, uint32_t* mask_slot, int lane,
-                                           uint64_t policy) {
+                                           uint64_t policy, bool dry = false) {
     const clo_half* bk;
     const clo_half* bv;
     int roff;
@@ -461,8 +477,9 @@ __device__ __forceinline__ void issue_tile(const Geo& geo, const int* gsm, const
         const int ro = __shfl_sync(FULL_MASK, roff, r) + chunk * 8;
         const bool v = (valid >> r) & 1u;
         const uint32_t dst = dst0 + 2 * i * ROW_BYTES + ((chunk ^ (r & 7)) << 4);
-        cp_async_16_hint(dst, bk + (v ? ro : 0), v ? 16 : 0, policy);
-        cp_async_16_hint(dst + KV_TILE_BYTES, bv + (v ? ro : 0), v ? 16 : 0, policy);
+        const int nb = (v && !dry) ? 16 : 0;  // dry: zero-fill, nothing read
+        cp_async_16_hint(dst, bk + (v ? ro : 0), nb, policy);
+        cp_async_16_hint(dst + KV_TILE_BYTES, bv + (v ? ro : 0), nb, policy);
     }
 }
 
@@ -563,8 +580,8 @@ __device__ __forceinline__ void load_q(const AttnOut& o, const Seg& sg, int lane
 }
 
 struct MergeSmem {
-    float* m;     // [WARPS][MAXG]
-    float* l;     // [WARPS][MAXG]
+    float* m;     // [MAXG][WARPS]
+    float* l;     // [MAXG][WARPS]
     int* bad;     // [WARPS]
     float* o;     // [WARPS][G][OSTRIDE]
 };
@@ -582,11 +599,11 @@ __device__ __forceinline__ void flush_segment(const AttnOut& o, const MergeSmem&
         l1 += __shfl_xor_sync(FULL_MASK, l1, off);
     }
     const int h0 = 2 * (lane & 3), h1 = h0 + 1;
-    if (lane < 4) {
-        ms.m[warp * MAXG + h0] = w.m0;
-        ms.m[warp * MAXG + h1] = w.m1;
-        ms.l[warp * MAXG + h0] = l0;
-        ms.l[warp * MAXG + h1] = l1;
+    if (lane < 4) {  // [head][warp] layout: one 16-byte load per head in the merge below
+        ms.m[h0 * ATTN_WARPS + warp] = w.m0;
+        ms.m[h1 * ATTN_WARPS + warp] = w.m1;
+        ms.l[h0 * ATTN_WARPS + warp] = l0;
+        ms.l[h1 * ATTN_WARPS + warp] = l1;
     }
     const int badw = static_cast<int>(__reduce_or_sync(FULL_MASK, static_cast<unsigned>(w.bad)));
     if (lane == 0) {
@@ -607,34 +624,58 @@ __device__ __forceinline__ void flush_segment(const AttnOut& o, const MergeSmem&
         }
     }
     __syncthreads();
-    int bad = force_bad ? 1 : 0;
-    for (int x = 0; x < ATTN_WARPS; ++x) bad |= ms.bad[x];
+    // Each thread combines four consecutive columns of one head with 16-byte
+    // shared loads: few load instructions matter here, because the other
+    // CTAs' copies keep the SM's memory pipeline busy and every shared load
+    // queues behind them.
+    static_assert(ATTN_WARPS == 4, "the merge reads the warps' (m, l) of a head as one float4");
+    const int4 bw = *reinterpret_cast<const int4*>(ms.bad);
+    const bool bad = force_bad || (bw.x | bw.y | bw.z | bw.w) != 0;
     const bool complete = sg.first >= c0 && sg.first + sg.ntiles <= c1;
-    for (int it = threadIdx.x; it < G * D; it += ATTN_THREADS) {
-        const int h = it >> 7, dd = it & (D - 1);
-        float M = -INFINITY;
-        for (int x = 0; x < ATTN_WARPS; ++x) M = fmaxf(M, ms.m[x * MAXG + h]);
-        float L = 0.f, O = 0.f;
+    for (int it = threadIdx.x; it < G * (D / 4); it += ATTN_THREADS) {
+        const int h = it / (D / 4), dd = (it % (D / 4)) * 4;
+        const float4 mv = *reinterpret_cast<const float4*>(ms.m + h * ATTN_WARPS);
+        const float4 lv = *reinterpret_cast<const float4*>(ms.l + h * ATTN_WARPS);
+        const float mx[4] = {mv.x, mv.y, mv.z, mv.w};
+        const float lx[4] = {lv.x, lv.y, lv.z, lv.w};
+        float4 ov[ATTN_WARPS];
+#pragma unroll
+        for (int x = 0; x < ATTN_WARPS; ++x)
+            ov[x] = *reinterpret_cast<const float4*>(ms.o + (x * G + h) * OSTRIDE + dd);
+        const float M = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
         if (M != -INFINITY) {
+#pragma unroll
             for (int x = 0; x < ATTN_WARPS; ++x) {
-                const float mw = ms.m[x * MAXG + h];
-                if (mw != -INFINITY) {
-                    const float e = fast_exp2(mw - M);
-                    L = fmaf(ms.l[x * MAXG + h], e, L);
-                    O = fmaf(ms.o[(x * G + h) * OSTRIDE + dd], e, O);
+                if (mx[x] != -INFINITY) {
+                    const float e = fast_exp2(mx[x] - M);
+                    L = fmaf(lx[x], e, L);
+                    O[0] = fmaf(ov[x].x, e, O[0]);
+                    O[1] = fmaf(ov[x].y, e, O[1]);
+                    O[2] = fmaf(ov[x].z, e, O[2]);
+                    O[3] = fmaf(ov[x].w, e, O[3]);
                 }
             }
         }
         const bool empty = !(L > 0.f);
         if (complete) {
             const size_t row = static_cast<size_t>(sg.b) * o.Hq + static_cast<size_t>(sg.kv) * G + h;
-            const float val = (bad || empty) ? 0.f : O / L;
-            o.out[row * D + dd] = __half_as_ushort(__float2half_rn(val));
+            uint32_t pk[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float v0 = (bad || empty) ? 0.f : O[2 * j] / L;
+                const float v1 = (bad || empty) ? 0.f : O[2 * j + 1] / L;
+                pk[j] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v0))) |
+                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v1))) << 16);
+            }
+            *reinterpret_cast<uint2*>(o.out + row * D + dd) = make_uint2(pk[0], pk[1]);
             if (o.lse != nullptr && dd == 0)
                 o.lse[row] = (bad || empty) ? -INFINITY : (M + log2f(L)) * LN2;
         } else {
             const size_t slot = slot_base + static_cast<size_t>(s);
-            o.ws_o[(slot * G + h) * D + dd] = empty ? 0.f : O / L;
+            const float4 r = empty ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                   : make_float4(O[0] / L, O[1] / L, O[2] / L, O[3] / L);
+            *reinterpret_cast<float4*>(o.ws_o + (slot * G + h) * D + dd) = r;
             if (dd == 0) o.ws_lse[slot * G + h] = bad ? INFINITY : (empty ? -INFINITY : M + log2f(L));
         }
     }
@@ -655,20 +696,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     int* gsm = reinterpret_cast<int*>(ms.o + ATTN_WARPS * o.G * OSTRIDE);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Dependents may start only once this grid has passed its own wait, so a
-    // dependent's code before its wait sees everything written before this
-    // kernel (the merge kernel runs a fused lookup there).
-    pdl_wait();
-    pdl_launch_dependents();
     // With a static layout (hybrid) the CTA ranges and the addresses of
-    // contiguous Persistent Cache tiles need no shared state, so the first of
-    // those copies are issued before the CTA reads persist_ids; the id round
-    // trip then overlaps the first data round trip.
+    // contiguous Persistent Cache tiles depend on the kernel parameters
+    // alone: they are worked out before the dependency wait, while the grid
+    // is resident early and its predecessor drains, and the first copies go
+    // out right after the wait, ahead of the persist_ids round trip.  Layouts
+    // that depend on device data (paged) set up after the wait.
     constexpr bool kEarly = Geo::kStaticLayout;
-    int ids_pre = 0;
-    if constexpr (kEarly) {
-        ids_pre = geo.ids_preload();
-    } else {
+    if constexpr (!kEarly) {
+        // Dependents may start only once this grid has passed its own wait,
+        // so a dependent's code before its wait sees everything written
+        // before this kernel (the merge kernel runs a fused lookup there).
+        pdl_wait();
+        pdl_launch_dependents();
         geo.cta_init(gsm, o.err_flag, blockIdx.x == 0);
         __syncthreads();
     }
@@ -692,7 +732,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
         }
         total += rl[p];
     }
-    if (total == 0) return;  // uniform over the CTA
+    if (!kEarly && total == 0) return;  // uniform over the CTA
     // Odd CTAs take their two ranges in the opposite order, so that half the
     // grid reads scattered Cache Buffer rows while the other half streams
     // the Persistent Cache: the part switch is not taken by every CTA at
@@ -723,21 +763,37 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     };
     const long long u_first = min(static_cast<long long>(warp), total - 1);
     int n_early = 0;
-    if (kEarly && pf == 0 && u_first < rl[0]) {
-        cursor_init(geo, gsm, tile_at(u_first), cur);  // part 0: the table's kv is not used
-#pragma unroll
-        for (int j = 0; j < ATTN_STAGES - 1; ++j) {
-            if (n_early == j && j < nj && warp + static_cast<long long>(j) * ATTN_WARPS < rl[0]) {
-                prefetch(j);
-                issue_tile(geo, gsm, pd, ring + j * STAGE_BYTES, my_masks + j, lane, kv_policy);
-                cp_async_commit();
-                ++n_early;
-            }
-        }
-    }
     if constexpr (kEarly) {
+        // The first tile of a CTA that starts on the Persistent Cache needs no
+        // device data.  Its copies are issued by one code path run twice:
+        // before the wait as zero-fill copies (no global reads; this brings
+        // the code and the parameters on chip while the predecessor drains),
+        // then for real once the wait has passed.
+        const bool early = pf == 0 && warp < rl[0] && ATTN_STAGES > 1;  // warp < rl[0]: nj > 0
+        if (early) {
+            cursor_init(geo, gsm, tile_at(u_first), cur);  // part 0: the table's kv is not used
+            prefetch(0);
+        }
+        int ids_pre = 0;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+                pdl_wait();  // dependents start only after this (see the paged branch above)
+                pdl_launch_dependents();
+                if (total == 0) return;  // uniform over the CTA
+                ids_pre = geo.ids_preload();
+            }
+            if (early) {
+                issue_tile(geo, gsm, pd, ring, my_masks, lane, kv_policy, pass == 0);
+                cp_async_commit();
+            }
+            if (pass == 0) cp_async_wait<0>();
+        }
+        n_early = early ? 1 : 0;
         geo.cta_init_with(gsm, o.err_flag, blockIdx.x == 0, ids_pre);
         __syncthreads();
+        if (Geo::kParts > 1 && rl[Geo::kParts - 1] > 0)
+            geo.prefetch_indices(gsm, ra[Geo::kParts - 1], rl[Geo::kParts - 1]);
     }
     const bool all_bad = geo.all_bad(gsm);
     if (n_early == 0) {

@@ -45,6 +45,12 @@ __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, 
                  : "memory");
 }
 
+// Hint: fetch the line holding `p` into L2 (no register result, never faults
+// on a valid address).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
