@@ -131,6 +131,7 @@ struct HybridGeo {
     long long n1;           // tiles in part 1 (B * (Hkv - Np) * tc)
 
     static constexpr int kParts = 2;
+    static constexpr bool kAheadAtFlush = false;
     // Shared scratch: [0] = ids valid flag, [1 .. Hkv] slot -> KV head,
     // [1 + Hkv .. 1 + 2 Hkv) staged persist_ids.
     static size_t smem_ints(int Hkv_, int /*B*/) { return 2 * static_cast<size_t>(Hkv_) + 4; }
@@ -364,6 +365,7 @@ struct PagedGeo {
         }
     }
     static constexpr int kParts = 1;
+    static constexpr bool kAheadAtFlush = true;
     static constexpr bool kStaticLayout = false;  // depends on ctx_len
     __device__ long long part_begin(int, const int*) const { return 0; }
     __device__ long long part_tiles(int, const int* sm) const { return sm[B]; }
@@ -813,6 +815,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
     if (ATTN_STAGES - 1 < nj) prefetch(ATTN_STAGES - 1);
 
     int jc = 0;
+    // ahead: the copies of tile jc + 1 went out before a segment flush (see below).
+    bool ahead = false;
     WarpState w;
 #pragma unroll 1
     for (int pi = 0; pi < Geo::kParts; ++pi) {
@@ -830,19 +834,41 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
             while (jc < nj) {
                 const long long t = tile_at(warp + static_cast<long long>(jc) * ATTN_WARPS);
                 if (t >= seg_end || t < sg.first) break;  // (a reversed CTA goes back to part 0)
-                cp_async_wait<ATTN_STAGES - 2>();
+                if (ahead)
+                    cp_async_wait<ATTN_STAGES - 1>();
+                else
+                    cp_async_wait<ATTN_STAGES - 2>();
                 __syncwarp();
                 const int jn = jc + ATTN_STAGES - 1;
-                if (jn < nj)
-                    issue_tile(geo, gsm, pd, ring + (jn % ATTN_STAGES) * STAGE_BYTES,
-                               my_masks + jn % ATTN_STAGES, lane, kv_policy);
-                cp_async_commit();
-                if (jn + 1 < nj) prefetch(jn + 1);
+                if (!ahead) {
+                    if (jn < nj)
+                        issue_tile(geo, gsm, pd, ring + (jn % ATTN_STAGES) * STAGE_BYTES,
+                                   my_masks + jn % ATTN_STAGES, lane, kv_policy);
+                    cp_async_commit();
+                    if (jn + 1 < nj) prefetch(jn + 1);
+                }
+                ahead = false;
                 const int st = jc % ATTN_STAGES;
                 const uint32_t mw = *reinterpret_cast<volatile uint32_t*>(my_masks + st);
                 w.bad |= static_cast<int>(mw >> 16);
                 compute_tile(ring + st * STAGE_BYTES, mw & 0xffffu, qb, o.scale_log2, w, lane);
                 ++jc;
+            }
+            // The warps reach a segment end up to a few microseconds apart and
+            // wait for each other in the flush.  The stage of the tile just
+            // computed is free, so with many short token sets (paged) the tile
+            // after the one in flight is issued into it first and each waiting
+            // warp keeps two tiles on the way.  With a few long sets (hybrid)
+            // this measured slower: the extra copies queue ahead of the
+            // flush's shared-memory loads.
+            if (Geo::kAheadAtFlush && ATTN_STAGES == 2 && !ahead && jc + 1 < nj) {
+                __syncwarp();
+                const int jn = jc + 1;
+                issue_tile(geo, gsm, pd, ring + (jn % ATTN_STAGES) * STAGE_BYTES,
+                           my_masks + jn % ATTN_STAGES, lane, kv_policy);
+                cp_async_commit();
+                if (jn + 1 < nj) prefetch(jn + 1);
+                ahead = true;
             }
             flush_segment(o, ms, w, sg, s, c0, c1, blockIdx.x + static_cast<size_t>(p) * C,
                           all_bad, warp, lane);
