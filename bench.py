@@ -109,8 +109,12 @@ class HybridWorkload:
             self.n_inst = int(min(8, max(2, math.ceil(2 ** 30 / per_layer))))
         self.inst = []
         s_all = []
+        n = cfg.B * cfg.Hkv
         for i in range(self.n_inst):
             li = i + 1000 * rank
+            # The lookup's outputs share one buffer (sim, miss list, miss count,
+            # flags), so the host reads them back with a single copy.
+            res = torch.empty(9 * n + 4, dtype=torch.uint8, device=dev)
             q, lab = wl.queries_and_labels(cfg, li, dev)
             has_cb = cfg.Np < cfg.Hkv
             cbK, cbV, idx = wl.cache_buffer(cfg, li, dev) if has_cb else (None, None, None)
@@ -123,10 +127,11 @@ class HybridWorkload:
                 pmask=torch.from_numpy(wl.persist_mask(cfg, li)).to(dev),
                 w=torch.from_numpy(s_np).to(dev),
                 out=torch.empty_like(q),
-                flag=torch.empty(cfg.B * cfg.Hkv, dtype=torch.uint8, device=dev),
-                sim=torch.empty(cfg.B * cfg.Hkv, dtype=torch.float32, device=dev),
-                miss=torch.empty(cfg.B * cfg.Hkv, dtype=torch.int32, device=dev),
-                nmiss=torch.zeros(1, dtype=torch.int32, device=dev)))
+                res=res,
+                sim=res[0:4 * n].view(torch.float32),
+                miss=res[4 * n:8 * n].view(torch.int32),
+                nmiss=res[8 * n:8 * n + 4].view(torch.int32).zero_(),
+                flag=res[8 * n + 4:9 * n + 4]))
         self.s = torch.from_numpy(np.concatenate(s_all)).to(dev)
         self.tau = torch.empty(self.n_inst * cfg.Hkv, dtype=torch.float32, device=dev)
         self.ws = torch.empty(clo.clo_hybrid_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.d),
@@ -229,10 +234,7 @@ class HybridWorkload:
         torch = self.torch
         self.h_q = [it["q"].cpu().pin_memory() for it in self.inst]
         self.h_out = [torch.empty_like(it["out"], device="cpu").pin_memory() for it in self.inst]
-        self.h_flag = [torch.empty_like(it["flag"], device="cpu").pin_memory() for it in self.inst]
-        self.h_sim = [torch.empty_like(it["sim"], device="cpu").pin_memory() for it in self.inst]
-        self.h_miss = [torch.empty_like(it["miss"], device="cpu").pin_memory() for it in self.inst]
-        self.h_nmiss = [torch.empty_like(it["nmiss"], device="cpu").pin_memory() for it in self.inst]
+        self.h_res = [torch.empty_like(it["res"], device="cpu").pin_memory() for it in self.inst]
         cfg = self.cfg
         self.e2e_h2d = self.L * cfg.B * cfg.Hq * cfg.d * HALF
         self.e2e_d2h = self.L * (cfg.B * cfg.Hq * cfg.d * HALF + cfg.B * cfg.Hkv * 9 + 4)
@@ -250,10 +252,7 @@ class HybridWorkload:
                 self._attention_lookup(step, l)
                 j = (step * self.L + l) % self.n_inst
                 self.h_out[j].copy_(self.inst[j]["out"], non_blocking=True)
-                self.h_flag[jn].copy_(nx["flag"], non_blocking=True)
-                self.h_sim[jn].copy_(nx["sim"], non_blocking=True)
-                self.h_miss[jn].copy_(nx["miss"], non_blocking=True)
-                self.h_nmiss[jn].copy_(nx["nmiss"], non_blocking=True)
+                self.h_res[jn].copy_(nx["res"], non_blocking=True)
             return
         for l in range(self.L):
             j = (step * self.L + l) % self.n_inst
@@ -265,10 +264,7 @@ class HybridWorkload:
             clo.clo_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"],
                                        it["pV"], it["pid"], it["out"], self.ws, err_flag=self.err)
             self.h_out[j].copy_(it["out"], non_blocking=True)
-            self.h_flag[j].copy_(it["flag"], non_blocking=True)
-            self.h_sim[j].copy_(it["sim"], non_blocking=True)
-            self.h_miss[j].copy_(it["miss"], non_blocking=True)
-            self.h_nmiss[j].copy_(it["nmiss"], non_blocking=True)
+            self.h_res[j].copy_(it["res"], non_blocking=True)
 
     def lookup_stats(self, reps: int = 50) -> dict:
         """The lookup on its own, after the timed region: hit rate and
