@@ -794,8 +794,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
         n_early = early ? 1 : 0;
         geo.cta_init_with(gsm, o.err_flag, blockIdx.x == 0, ids_pre);
         __syncthreads();
+        // At most 128 tiles (8 KB of indices) a CTA: enough for the ranges of
+        // these workloads, and bounded for very long ones.
         if (Geo::kParts > 1 && rl[Geo::kParts - 1] > 0)
-            geo.prefetch_indices(gsm, ra[Geo::kParts - 1], rl[Geo::kParts - 1]);
+            geo.prefetch_indices(gsm, ra[Geo::kParts - 1], min(rl[Geo::kParts - 1], 128ll));
     }
     const bool all_bad = geo.all_bad(gsm);
     if (n_early == 0) {

@@ -36,6 +36,19 @@ __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_THREADS,
     lookup_cluster<LK_WARPS>(p, miss_sm, &cta_misses);
 }
 
+// The same with 16 warps per CTA, for more groups than the narrow form has
+// warps: every warp then scores at most one group per CTA pass, so the
+// launch is one round trip for the queries and labels instead of several.
+constexpr int LK_WIDE_THREADS = 512;
+__global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_WIDE_THREADS, 1)
+    lookup_update_wide_kernel(const LookupParams p) {
+    extern __shared__ uint8_t miss_sm[];
+    __shared__ int cta_misses;
+    pdl_launch_dependents();
+    pdl_wait();
+    lookup_cluster<LK_WIDE_THREADS / 32>(p, miss_sm, &cta_misses);
+}
+
 }  // namespace clo
 
 using namespace clo;
@@ -72,9 +85,10 @@ extern "C" clo_status clo_lookup_update(const clo_half* q, clo_half* labels, con
                                              flag, sim, miss_list, miss_count, p);
     if (st != CLO_OK) return st;
     const int per_cta = lookup_smem_bytes(B, Hkv);
-    if (!prepare_kernel(reinterpret_cast<const void*>(lookup_update_kernel), per_cta))
-        return CLO_ERR_CUDA;
-    return launch_pdl(lookup_update_kernel, dim3(LK_CLUSTER), dim3(LK_THREADS),
+    const bool wide = static_cast<long long>(B) * Hkv > static_cast<long long>(LK_CLUSTER) * LK_WARPS;
+    auto* kern = wide ? lookup_update_wide_kernel : lookup_update_kernel;
+    if (!prepare_kernel(reinterpret_cast<const void*>(kern), per_cta)) return CLO_ERR_CUDA;
+    return launch_pdl(kern, dim3(LK_CLUSTER), dim3(wide ? LK_WIDE_THREADS : LK_THREADS),
                       static_cast<size_t>(per_cta), stream, p) == cudaSuccess
                ? CLO_OK
                : CLO_ERR_CUDA;
