@@ -84,6 +84,21 @@ def test_lookup_many_groups_half_miss():
     compare(q, lab, w, tau, pm)
 
 
+@pytest.mark.parametrize("B", [4, 5, 16, 17])
+def test_lookup_cta_width_boundary(B):
+    """32 groups run on 4-warp CTAs, 40 and more on 16-warp CTAs (one group a
+    warp per pass); both sides of the switch, with about half of them missing."""
+    rng = np.random.Generator(np.random.PCG64(50 + B))
+    Hq, Hkv = 32, 8
+    lab = rng.standard_normal((B, Hq, 128)).astype(np.float16)
+    q = (0.5 * lab + rng.standard_normal((B, Hq, 128))).astype(np.float16)
+    w = rng.uniform(0, 1, Hq).astype(np.float32)
+    tau = np.full(Hkv, 0.447, dtype=np.float32)
+    pm = np.zeros(Hkv, dtype=np.uint8)
+    pm[5] = 1
+    compare(q, lab, w, tau, pm)
+
+
 def test_lookup_mha_and_gqa8():
     rng = np.random.Generator(np.random.PCG64(6))
     for (B, Hq, Hkv) in [(5, 32, 32), (3, 64, 8), (257, 8, 8)]:
