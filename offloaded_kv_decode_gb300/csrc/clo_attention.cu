@@ -75,6 +75,11 @@ constexpr int OSTRIDE = D + 4;  // padded merge-area row (floats): conflict-free
 #ifndef CLO_ATTN_CTAS_PER_SM
 #define CLO_ATTN_CTAS_PER_SM 3
 #endif
+// Persistent Cache tiles a CTA that starts on the Cache Buffer brings into L2
+// at its start (see attn_split_kernel).
+#ifndef CLO_ATTN_EARLY_L2_TILES
+#define CLO_ATTN_EARLY_L2_TILES 8
+#endif
 constexpr int ATTN_WARPS = CLO_ATTN_WARPS;
 constexpr int ATTN_CTAS_PER_SM = CLO_ATTN_CTAS_PER_SM;
 constexpr int ATTN_STAGES = CLO_ATTN_STAGES;
@@ -255,6 +260,21 @@ struct HybridGeo {
         return g;
     }
     __device__ bool all_bad(const int* sm) const { return sm[0] == 0; }
+    // Brings the K and V rows of Persistent Cache tiles [t0, t0 + n) (part 0)
+    // into L2 with an evict-last hint; needs no device data.
+    __device__ void prefetch_persistent(long long t0, long long n) const {
+        constexpr int kLines = KV_TILE_BYTES / 128;  // 128-byte lines of K (or V) in a tile
+        for (long long i = threadIdx.x; i < n * 2 * kLines; i += blockDim.x) {
+            const long long t = t0 + i / (2 * kLines);
+            const int line = static_cast<int>(i % (2 * kLines));
+            const int s = static_cast<int>(t / tp);
+            const int tile_in = static_cast<int>(t - static_cast<long long>(s) * tp);
+            const int row = tile_in * TILE + (line % kLines) / 2;  // two lines a 256-byte row
+            if (row >= T) continue;
+            const clo_half* base = (line < kLines ? pK : pV) + static_cast<long long>(s) * T * D;
+            prefetch_l2_keep(base + static_cast<long long>(row) * D + (line & 1) * 64);
+        }
+    }
     // Brings the Cache Buffer indices of tiles [t0, t0 + n) of part 1 into L2
     // (the lines holding each tile's first and last index), so that the
     // per-tile index loads, issued one pipeline step ahead of their copies,
@@ -784,6 +804,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, ATTN_CTAS_PER_SM)
                 pdl_launch_dependents();
                 if (total == 0) return;  // uniform over the CTA
                 ids_pre = geo.ids_preload();
+                // A CTA that starts on the Cache Buffer waits two round trips
+                // (persist_ids, then its indices) before its first copies, while
+                // the DRAM has room.  It uses them to bring the first tiles of
+                // its Persistent Cache range into L2; it reads them from there
+                // when it gets to them.
+                if (Geo::kParts > 1 && pf == 1 && rl[0] > 0 && CLO_ATTN_EARLY_L2_TILES > 0)
+                    geo.prefetch_persistent(ra[0], min(rl[0], static_cast<long long>(CLO_ATTN_EARLY_L2_TILES)));
             }
             if (early) {
                 issue_tile(geo, gsm, pd, ring, my_masks, lane, kv_policy, pass == 0);
