@@ -289,10 +289,11 @@ clo_status clo_hybrid_decode_attn_lookup(
 
 /*
  * clo_hybrid_decode_attn_noalloc -- clo_hybrid_decode_attn for callers that
- * cannot allocate device memory: code running while its stream is captured
- * into a CUDA graph (an allocation would break the capture), engines that own
- * all device memory through their own pool, or deployments that forbid
- * allocation after start-up.  The pages have no counterpart: this is a
+ * cannot allocate device memory: serving engines that reserve all free device
+ * memory for their own pool at start-up (so a later cudaMalloc fails or
+ * fragments that pool), deployments that forbid allocation after start-up,
+ * and host programs that reach this library through its C ABI alone, with no
+ * allocator of their own.  The pages have no counterpart: this is a
  * deployment variant of the same computation.
  * Same arguments, layouts and results as clo_hybrid_decode_attn, without the
  * workspace: the split-KV scratch is a fixed array of
@@ -305,9 +306,9 @@ clo_status clo_hybrid_decode_attn_lookup(
  *    stream capture.  CLO_ERR_CUDA if the lookup fails.
  *  - It never calls cudaMalloc, cudaFree or any allocating routine.
  *  - All calls share the one array and it keeps the previous call's
- *    contents; nothing in it needs to start at zero.  Calls that overlap on
- *    the GPU (concurrent streams, or devices sharing a context) race on it:
- *    serialise them.
+ *    contents; nothing in it needs to start at zero.  Calls on one device
+ *    that overlap on the GPU (on concurrent streams) race on it: serialise
+ *    them.  Each device has its own copy of the array.
  */
 clo_status clo_hybrid_decode_attn_noalloc(const clo_half* q, const clo_half* cbK,
                                           const clo_half* cbV, const int32_t* idx, int k, int C,

@@ -424,11 +424,11 @@ def clo_hybrid_decode_attn_noalloc(q: torch.Tensor, cbK: Optional[torch.Tensor],
                                    scale: Optional[float] = None, num_ctas: int = 0,
                                    events: Optional[Sequence] = None, stream=None):
     """clo_hybrid_decode_attn without a caller workspace, for callers that
-    cannot allocate device memory at call time (e.g. under CUDA-graph capture
-    or with an engine-owned memory pool): the library's fixed 8 MiB scratch is
-    used instead.  Raises CloError(CLO_ERR_WORKSPACE) for problems needing
-    more; calls that overlap on the GPU share that scratch and must be
-    serialised."""
+    cannot allocate device memory at call time (an engine whose own pool holds
+    all free device memory, allocation frozen after start-up): the library's
+    fixed 8 MiB scratch is used instead.  Raises CloError(CLO_ERR_WORKSPACE)
+    for problems needing more; calls on one device that overlap on the GPU
+    share that scratch and must be serialised."""
     pq = _dev(q, "q", torch.float16, 3)
     B, Hq, d = q.shape
     Np = 0 if persist_ids is None else persist_ids.numel()

@@ -1417,11 +1417,11 @@ extern "C" clo_status clo_paged_decode_attn(const clo_half* q, const clo_half* k
 }
 
 // ---------------------------------------------------------------- no-allocation variant
-// Some callers cannot allocate device memory when they run this path: code
-// that executes while its stream is being captured into a CUDA graph (an
-// allocation there fails the capture), engines that hand every byte of the
-// GPU to their own pool and forbid outside allocations, and deployments that
-// freeze allocation after start-up.  clo_hybrid_decode_attn_noalloc serves
+// Some callers cannot allocate device memory when they run this path: serving
+// engines that hand every free byte of the GPU to their own pool at start-up
+// and forbid outside allocations, deployments that freeze allocation after
+// start-up, and host programs that reach the library through its C ABI alone,
+// with no allocator of their own.  clo_hybrid_decode_attn_noalloc serves
 // them: its split-KV scratch is the fixed array below, part of the library
 // image, which every GPU that loads the library keeps until the process exits.
 namespace clo {

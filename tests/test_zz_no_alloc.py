@@ -1,9 +1,9 @@
 """The no-allocation hybrid attention entry point (GPU).
 
 clo_hybrid_decode_attn_noalloc exists for callers that cannot allocate device
-memory when they run the decode path -- code running under CUDA-graph stream
-capture, engines whose own pool owns all device memory, deployments that
-freeze allocation after start-up.  It must give the same results as the
+memory when they run the decode path -- engines whose own pool holds all
+free device memory, deployments that freeze allocation after start-up, host
+programs with no allocator of their own.  It must give the same results as the
 workspace entry point; here both are called through the C ABI on the same
 inputs, twice in a row for the fixed-scratch variant (the scratch keeps the
 previous call's contents), and compared at the parity tolerance.  This file is
