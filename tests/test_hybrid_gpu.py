@@ -101,6 +101,14 @@ def test_split_count_independence():
     assert np.array_equal(again, outs[-1]), "same launch must be bit-reproducible"
 
 
+@pytest.mark.parametrize("num_ctas", [7, 37, 100])
+def test_ranges_cross_segments_in_both_parts(num_ctas):
+    """Segment boundaries crossed in both parts (8 batch rows; 2 persistent heads
+    of 128 tiles and 6 Cache Buffer heads of 21 tiles each), so some CTAs flush
+    three to five segments: every partial lands in the slot the merge reads."""
+    check_small(small_case(13, 8, 32, 8, 2048, 330, 2), num_ctas, "weighted cut")
+
+
 def test_tiny_config_from_generator():
     cfg = wl.CONFIGS["tiny"]
     q, _ = wl.queries_and_labels(cfg, 0, "cpu")
