@@ -84,6 +84,30 @@ int clo_version(void);
  * zero, CLO_ERR_BAD_INDEX when any CLO_FLAG_* bit is set. */
 clo_status clo_check_error_flag(int32_t host_err_flag);
 
+/* One copy of `bytes` bytes from src to dst. */
+typedef struct clo_copy {
+    void* dst;
+    const void* src;
+    size_t bytes;
+} clo_copy;
+
+/*
+ * clo_copy_async -- issues copies[0..n) in order on `stream`, one
+ * cudaMemcpyAsync each (direction inferred from the pointers), so a caller
+ * that holds a step's inputs or results in host memory moves them with one
+ * call instead of one per buffer.  The pages have no counterpart: it is the
+ * host-buffer edge of this library, and nothing in it computes.
+ *  - Host buffers must be pinned (page-locked) for the copies to be
+ *    asynchronous; pageable memory makes the call wait for the copy.  The
+ *    caller keeps every buffer alive and unchanged until the stream reaches
+ *    the copy.
+ *  - Copies with bytes == 0 are skipped.  n < 0, copies == NULL with n > 0,
+ *    or a NULL dst/src in a non-empty copy give CLO_ERR_INVALID_ARG before
+ *    anything is issued; a failed cudaMemcpyAsync gives CLO_ERR_CUDA (the
+ *    copies before it stay issued).
+ */
+clo_status clo_copy_async(const clo_copy* copies, int n, cudaStream_t stream);
+
 /*
  * clo_thresholds -- per-KV-head similarity thresholds, CLO Eqs. 7-9:
  *     theta* = arccos(eta), lambda = s^n, theta = lambda*theta* + (1-lambda)*pi,

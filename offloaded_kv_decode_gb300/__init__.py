@@ -54,6 +54,7 @@ _SIGS = {
     "clo_status_string": ([_I], ctypes.c_char_p),
     "clo_version": ([], _I),
     "clo_check_error_flag": ([ctypes.c_int32], _I),
+    "clo_copy_async": ([_P, _I, _P], _I),
     "clo_thresholds": ([_P, _I, _I, _F, _F, _P, _P], _I),
     "clo_lookup_update": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "clo_fill_cache_buffer": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P,
@@ -163,19 +164,113 @@ def _opts(num_ctas: int, events) -> Optional[AttnOpts]:
     return AttnOpts(int(num_ctas), eb or None, ee or None)
 
 
+_BYREF = type(ctypes.byref(ctypes.c_int()))
+
+
+class PreparedCall:
+    """One libclo call whose arguments were checked and marshalled once.
+
+    Calling it issues the same C call again (same buffers; their contents may
+    change between calls) without redoing the Python-side checks, for loops
+    that re-run a decode step on fixed buffers.  It holds references to its
+    tensors, so they stay alive as long as the object does.  The stream is
+    the one given to the ``prepare_*`` function, else the current stream at
+    each call.
+    """
+
+    __slots__ = ("_fn", "_args", "_what", "_keep", "_stream")
+
+    def __init__(self, what: str, args: tuple, keep: tuple, stream=None):
+        fn = getattr(lib(), what)
+        types = fn.argtypes[:-1]  # the last argument is the stream
+        if len(types) != len(args):
+            raise CloError(f"{what}: {len(args)} arguments for {len(types)}", CLO_ERR_INVALID_ARG)
+        self._fn = fn
+        self._args = tuple(a if isinstance(a, _BYREF) else t(a) for t, a in zip(types, args))
+        self._what = what
+        self._keep = keep
+        self._stream = None if stream is None else _stream(stream)
+
+    def __call__(self):
+        st = self._stream
+        if st is None:
+            st = torch.cuda.current_stream().cuda_stream
+        status = self._fn(*self._args, st)
+        if status != CLO_OK:
+            _check(status, self._what)
+
+
+def _run(call, stream):
+    """Issues a (what, args, keep) call once on `stream`."""
+    what, args, _ = call
+    _check(getattr(lib(), what)(*args, _stream(stream)), what)
+
+
+# ---------------------------------------------------------------- host-buffer copies
+
+class CloCopy(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+def _copies_call(pairs):
+    """pairs: (dst, src) tensors, one on the GPU and the other in pinned host memory,
+    contiguous, with the same number of bytes."""
+    pairs = list(pairs)
+    arr = (CloCopy * max(len(pairs), 1))()
+    for i, (dst, src) in enumerate(pairs):
+        if isinstance(dst, torch.Tensor) and isinstance(src, torch.Tensor) and \
+                dst.numel() == 0 and src.numel() == 0:
+            arr[i] = CloCopy(None, None, 0)  # nothing to move
+            continue
+        for t, name in ((dst, "dst"), (src, "src")):
+            if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+                raise CloError(f"copy {i}: {name} must be a contiguous tensor", CLO_ERR_INVALID_ARG)
+            if not t.is_cuda and not t.is_pinned():
+                raise CloError(f"copy {i}: {name} must be a CUDA tensor or pinned host memory",
+                               CLO_ERR_INVALID_ARG)
+        if dst.is_cuda == src.is_cuda:
+            raise CloError(f"copy {i}: one side must be host memory and the other CUDA memory",
+                           CLO_ERR_INVALID_ARG)
+        nb = dst.numel() * dst.element_size()
+        if nb != src.numel() * src.element_size():
+            raise CloError(f"copy {i}: dst and src sizes differ", CLO_ERR_INVALID_ARG)
+        arr[i] = CloCopy(dst.data_ptr(), src.data_ptr(), nb)
+    return "clo_copy_async", (ctypes.addressof(arr), len(pairs)), (arr, pairs)
+
+
+def clo_copy_async(pairs: Sequence, stream=None):
+    """Issues the copies (dst, src) in order on the stream (pinned host <-> CUDA)."""
+    _run(_copies_call(pairs), stream)
+
+
+def prepare_copies(pairs: Sequence, stream=None) -> PreparedCall:
+    """clo_copy_async on fixed buffers, checked once (see PreparedCall)."""
+    what, args, keep = _copies_call(pairs)
+    return PreparedCall(what, args, keep, stream)
+
+
 # ---------------------------------------------------------------- thresholds
 
 def clo_thresholds(s: torch.Tensor, tau: torch.Tensor, group: int = 1, eta: float = 0.8,
                    n_exp: float = 3.0, stream=None) -> torch.Tensor:
     """tau[g] = cos(lambda*arccos(eta) + (1-lambda)*pi), lambda = mean(s of group g)^n."""
+    _run(_thresholds_call(s, tau, group, eta, n_exp), stream)
+    return tau
+
+
+def prepare_thresholds(s, tau, group: int = 1, eta: float = 0.8, n_exp: float = 3.0,
+                       stream=None) -> PreparedCall:
+    """clo_thresholds on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_thresholds_call(s, tau, group, eta, n_exp), stream)
+
+
+def _thresholds_call(s, tau, group, eta, n_exp):
     ps = _dev(s, "s", torch.float32)
     pt = _dev(tau, "tau", torch.float32)
     n_kv = tau.numel()
     if s.numel() != n_kv * group:
         raise CloError("s must hold tau.numel()*group scores", CLO_ERR_INVALID_ARG)
-    _check(lib().clo_thresholds(ps, n_kv, group, eta, n_exp, pt, _stream(stream)),
-           "clo_thresholds")
-    return tau
+    return ("clo_thresholds", (ps, n_kv, int(group), float(eta), float(n_exp), pt), (s, tau))
 
 
 # ---------------------------------------------------------------- lookup
@@ -206,8 +301,21 @@ def clo_lookup_update(q: torch.Tensor, labels: torch.Tensor, w_q: torch.Tensor,
                       flag: torch.Tensor, sim: torch.Tensor, miss_list: torch.Tensor,
                       miss_count: torch.Tensor, stream=None):
     """Fused head-wise cache lookup + Eq. 10 + label update (labels updated in place)."""
+    _run(_lookup_call(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count),
+         stream)
+
+
+def prepare_lookup_update(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list,
+                          miss_count, stream=None) -> PreparedCall:
+    """clo_lookup_update on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_lookup_call(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list,
+                                      miss_count), stream)
+
+
+def _lookup_call(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count):
     a = _lookup_args(q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count)
-    _check(lib().clo_lookup_update(*a, _stream(stream)), "clo_lookup_update")
+    return ("clo_lookup_update", a,
+            (q, labels, w_q, tau_kv, persist_mask, flag, sim, miss_list, miss_count))
 
 
 # ---------------------------------------------------------------- offline plan
@@ -246,6 +354,16 @@ def clo_topk_retrieve(q: torch.Tensor, K: torch.Tensor, k: int, idx: torch.Tenso
     """Per KV head, the k keys with the largest (sum of the group's queries) . K_t,
     ties to the lower token, ascending: q [B][Hq][d], K [B][Hkv][T][d] fp16,
     idx [B][Hkv][k] int32 output."""
+    _run(_topk_call(q, K, k, idx, workspace, num_ctas, events), stream)
+
+
+def prepare_topk_retrieve(q, K, k: int, idx, workspace, num_ctas: int = 0, events=None,
+                          stream=None) -> PreparedCall:
+    """clo_topk_retrieve on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_topk_call(q, K, k, idx, workspace, num_ctas, events), stream)
+
+
+def _topk_call(q, K, k, idx, workspace, num_ctas, events):
     pq = _dev(q, "q", torch.float16, 3)
     pk = _dev(K, "K", torch.float16, 4)
     pi = _dev(idx, "idx", torch.int32, 3)
@@ -255,9 +373,10 @@ def clo_topk_retrieve(q: torch.Tensor, K: torch.Tensor, k: int, idx: torch.Tenso
     if K.shape[0] != B or K.shape[3] != d or tuple(idx.shape) != (B, Hkv, k):
         raise CloError("top-k shapes do not match", CLO_ERR_INVALID_ARG)
     opts = _opts(num_ctas, events)
-    _check(lib().clo_topk_retrieve(pq, pk, B, Hq, Hkv, T, d, int(k), pi, pw, workspace.numel(),
-                                   ctypes.byref(opts) if opts is not None else None,
-                                   _stream(stream)), "clo_topk_retrieve")
+    return ("clo_topk_retrieve",
+            (pq, pk, B, Hq, Hkv, T, d, int(k), pi, pw, workspace.numel(),
+             ctypes.byref(opts) if opts is not None else None),
+            (q, K, idx, workspace, opts))
 
 
 # ---------------------------------------------------------------- miss-path fill
@@ -272,6 +391,20 @@ def clo_fill_cache_buffer(srcK: torch.Tensor, srcV: torch.Tensor, tok: torch.Ten
     Buffer (cbK/cbV [B][Hkv][C][d]) at slot[b][g][j] (tok itself when slot is
     None); tok/slot [B][Hkv][k] int32, miss_list/miss_count as written by
     clo_lookup_update."""
+    _run(_fill_call(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag, num_ctas,
+                    events), stream)
+
+
+def prepare_fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count,
+                              err_flag=None, num_ctas: int = 0, events=None,
+                              stream=None) -> PreparedCall:
+    """clo_fill_cache_buffer on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_fill_call(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count,
+                                    err_flag, num_ctas, events), stream)
+
+
+def _fill_call(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag, num_ctas,
+               events):
     ps = _dev_or_pinned(srcK, "srcK", torch.float16, 4)
     pv = _dev_or_pinned(srcV, "srcV", torch.float16, 4)
     B, Hkv, T, d = srcK.shape
@@ -290,9 +423,10 @@ def clo_fill_cache_buffer(srcK: torch.Tensor, srcV: torch.Tensor, tok: torch.Ten
     pmc = _dev(miss_count, "miss_count", torch.int32)
     pe = _dev(err_flag, "err_flag", torch.int32, optional=True)
     opts = _opts(num_ctas, events)
-    _check(lib().clo_fill_cache_buffer(ps, pv, T, pt, psl, k, pk, pcv, C, pml, pmc, B, Hkv, d,
-                                       pe, None if opts is None else ctypes.byref(opts),
-                                       _stream(stream)), "clo_fill_cache_buffer")
+    return ("clo_fill_cache_buffer",
+            (ps, pv, T, pt, psl, k, pk, pcv, C, pml, pmc, B, Hkv, d, pe,
+             None if opts is None else ctypes.byref(opts)),
+            (srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag, opts))
 
 
 # ---------------------------------------------------------------- attention
@@ -322,11 +456,24 @@ def clo_hybrid_decode_attn(q: torch.Tensor, cbK: Optional[torch.Tensor],
     fp32 (optional); workspace: a CUDA uint8 tensor of at least
     clo_hybrid_workspace_size(...) bytes.
     """
+    _run(_hybrid_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale,
+                      num_ctas, events), stream)
+
+
+def prepare_hybrid_decode_attn(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse=None,
+                               err_flag=None, scale=None, num_ctas: int = 0, events=None,
+                               stream=None) -> PreparedCall:
+    """clo_hybrid_decode_attn on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_hybrid_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse,
+                                      err_flag, scale, num_ctas, events), stream)
+
+
+def _hybrid_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale,
+                 num_ctas, events):
     a = _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale)
     opts = _opts(num_ctas, events)
-    _check(lib().clo_hybrid_decode_attn(
-        *a, ctypes.byref(opts) if opts is not None else None, _stream(stream)),
-        "clo_hybrid_decode_attn")
+    return ("clo_hybrid_decode_attn", a + (ctypes.byref(opts) if opts is not None else None,),
+            (q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, opts))
 
 
 def clo_hybrid_decode_attn_lookup(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace,
@@ -337,6 +484,27 @@ def clo_hybrid_decode_attn_lookup(q, cbK, cbV, idx, pK, pV, persist_ids, out, wo
     """clo_hybrid_decode_attn for this layer and clo_lookup_update for the next
     layer (same B, Hq, Hkv) in one launch sequence; the results equal the two
     separate calls."""
+    _run(_hybrid_lookup_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, q_next,
+                             labels_next, w_q_next, tau_next, persist_mask_next, flag_next,
+                             sim_next, miss_list_next, miss_count_next, lse, err_flag, scale,
+                             num_ctas, events), stream)
+
+
+def prepare_hybrid_decode_attn_lookup(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace,
+                                      q_next, labels_next, w_q_next, tau_next, persist_mask_next,
+                                      flag_next, sim_next, miss_list_next, miss_count_next,
+                                      lse=None, err_flag=None, scale=None, num_ctas: int = 0,
+                                      events=None, stream=None) -> PreparedCall:
+    """clo_hybrid_decode_attn_lookup on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_hybrid_lookup_call(
+        q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, q_next, labels_next, w_q_next,
+        tau_next, persist_mask_next, flag_next, sim_next, miss_list_next, miss_count_next, lse,
+        err_flag, scale, num_ctas, events), stream)
+
+
+def _hybrid_lookup_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, q_next,
+                        labels_next, w_q_next, tau_next, persist_mask_next, flag_next, sim_next,
+                        miss_list_next, miss_count_next, lse, err_flag, scale, num_ctas, events):
     a = _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale)
     b = _lookup_args(q_next, labels_next, w_q_next, tau_next, persist_mask_next, flag_next,
                      sim_next, miss_list_next, miss_count_next)
@@ -344,10 +512,12 @@ def clo_hybrid_decode_attn_lookup(q, cbK, cbV, idx, pK, pV, persist_ids, out, wo
         raise CloError("the next layer's lookup must have this layer's B, Hq, Hkv, d",
                        CLO_ERR_INVALID_ARG)
     opts = _opts(num_ctas, events)
-    _check(lib().clo_hybrid_decode_attn_lookup(
-        *a, b[0], b[1], b[2], b[3], b[4], b[9], b[10], b[11], b[12],
-        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
-        "clo_hybrid_decode_attn_lookup")
+    return ("clo_hybrid_decode_attn_lookup",
+            a + (b[0], b[1], b[2], b[3], b[4], b[9], b[10], b[11], b[12],
+                 ctypes.byref(opts) if opts is not None else None),
+            (q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, q_next, labels_next, w_q_next,
+             tau_next, persist_mask_next, flag_next, sim_next, miss_list_next, miss_count_next,
+             lse, err_flag, opts))
 
 
 def _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale):
@@ -386,6 +556,20 @@ def clo_paged_decode_attn(q: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor,
                           events: Optional[Sequence] = None, stream=None):
     """Paged decode attention: q [B][Hq][d]; kc/vc [num_blocks][Hkv][16][d];
     block_table [B][max_blocks] int32; ctx_len [B] int32."""
+    _run(_paged_call(q, kc, vc, block_table, ctx_len, out, workspace, lse, err_flag, scale,
+                     num_ctas, events), stream)
+
+
+def prepare_paged_decode_attn(q, kc, vc, block_table, ctx_len, out, workspace, lse=None,
+                              err_flag=None, scale=None, num_ctas: int = 0, events=None,
+                              stream=None) -> PreparedCall:
+    """clo_paged_decode_attn on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_paged_call(q, kc, vc, block_table, ctx_len, out, workspace, lse,
+                                     err_flag, scale, num_ctas, events), stream)
+
+
+def _paged_call(q, kc, vc, block_table, ctx_len, out, workspace, lse, err_flag, scale, num_ctas,
+                events):
     pq = _dev(q, "q", torch.float16, 3)
     B, Hq, d = q.shape
     pk = _dev(kc, "kc", torch.float16, 4)
@@ -403,11 +587,11 @@ def clo_paged_decode_attn(q: torch.Tensor, kc: torch.Tensor, vc: torch.Tensor,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     opts = _opts(num_ctas, events)
-    _check(lib().clo_paged_decode_attn(
-        pq, pk, pv, pbt, block_table.shape[1], pcl, num_blocks, B, Hq, Hkv, d, bs,
-        float(scale), pout, plse, pws, workspace.numel(), perr,
-        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
-        "clo_paged_decode_attn")
+    return ("clo_paged_decode_attn",
+            (pq, pk, pv, pbt, block_table.shape[1], pcl, num_blocks, B, Hq, Hkv, d, bs,
+             float(scale), pout, plse, pws, workspace.numel(), perr,
+             ctypes.byref(opts) if opts is not None else None),
+            (q, kc, vc, block_table, ctx_len, out, workspace, lse, err_flag, opts))
 
 
 def clo_hybrid_noalloc_max_scratch() -> int:

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import offloaded_kv_decode_gb300 as clo
 from offloaded_kv_decode_gb300 import build as libbuild
@@ -28,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 16, names
+    assert len(names) == 17, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -39,6 +40,24 @@ def test_status_helpers(L):
     assert clo.version() >= 100
     assert clo.check_error_flag(0) == clo.CLO_OK
     assert clo.check_error_flag(clo.FLAG_BAD_INDEX | clo.FLAG_BAD_PERSIST) == clo.CLO_ERR_BAD_INDEX
+
+
+def test_copy_async_validates_before_issuing(L):
+    """clo_copy_async rejects bad lists before any CUDA call (none is made here)."""
+    assert L.clo_copy_async(None, 0, None) == clo.CLO_OK
+    assert L.clo_copy_async(None, 1, None) == clo.CLO_ERR_INVALID_ARG
+    arr = (clo.CloCopy * 2)(clo.CloCopy(None, None, 0), clo.CloCopy(None, 16, 8))
+    assert L.clo_copy_async(ctypes.addressof(arr), -1, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_copy_async(ctypes.addressof(arr), 2, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_copy_async(ctypes.addressof(arr), 1, None) == clo.CLO_OK  # empty copy skipped
+
+
+def test_copy_pairs_checked_in_python():
+    a = torch.zeros(4)
+    with pytest.raises(clo.CloError):  # pageable host memory on both sides
+        clo.prepare_copies([(a, torch.zeros(4))])
+    what, args, _ = clo._copies_call([(torch.empty(0), torch.empty(0))])  # empty: skipped
+    assert what == "clo_copy_async" and args[1] == 1
 
 
 def test_workspace_size_formula(L):
