@@ -92,19 +92,26 @@ typedef struct clo_copy {
 } clo_copy;
 
 /*
- * clo_copy_async -- issues copies[0..n) in order on `stream`, one
- * cudaMemcpyAsync each (direction inferred from the pointers), so a caller
+ * clo_copy_async -- makes the copies copies[0..n) on `stream`, so a caller
  * that holds a step's inputs or results in host memory moves them with one
  * call instead of one per buffer.  The pages have no counterpart: it is the
  * host-buffer edge of this library, and nothing in it computes.
- *  - Host buffers must be pinned (page-locked) for the copies to be
- *    asynchronous; pageable memory makes the call wait for the copy.  The
- *    caller keeps every buffer alive and unchanged until the stream reaches
- *    the copy.
+ *  - Copies between memory the GPU can address (device or managed memory,
+ *    pinned host memory) that are 16-byte aligned and a multiple of 16 bytes
+ *    long are made by a libclo kernel, up to 16 of them a launch; the SMs read
+ *    and write host memory over the host link.  That kernel chains with the
+ *    libclo kernels before and after it like they chain with each other.  Any
+ *    other copy is one cudaMemcpyAsync (pageable host memory makes that wait
+ *    for the copy).
+ *  - The copies of one call may run at the same time: a list in which one
+ *    copy writes bytes that another reads or writes (or a copy onto itself)
+ *    gives CLO_ERR_INVALID_ARG.  Calls are ordered on the stream as usual.
+ *  - The caller keeps every buffer alive and unchanged until the stream
+ *    reaches the copy.
  *  - Copies with bytes == 0 are skipped.  n < 0, copies == NULL with n > 0,
  *    or a NULL dst/src in a non-empty copy give CLO_ERR_INVALID_ARG before
- *    anything is issued; a failed cudaMemcpyAsync gives CLO_ERR_CUDA (the
- *    copies before it stay issued).
+ *    anything is issued; a failed launch or cudaMemcpyAsync gives
+ *    CLO_ERR_CUDA (the copies before it stay issued).
  */
 clo_status clo_copy_async(const clo_copy* copies, int n, cudaStream_t stream);
 

@@ -1,5 +1,4 @@
-// clo_api.cu -- status helpers and the host-buffer copy call of the libclo
-// C ABI (host only).
+// clo_api.cu -- status helpers of the libclo C ABI (host only).
 #include "clo.h"
 
 extern "C" const char* clo_status_string(clo_status s) {
@@ -18,18 +17,4 @@ extern "C" int clo_version(void) { return 10200; }  // 1.2.0
 
 extern "C" clo_status clo_check_error_flag(int32_t host_err_flag) {
     return host_err_flag == 0 ? CLO_OK : CLO_ERR_BAD_INDEX;
-}
-
-extern "C" clo_status clo_copy_async(const clo_copy* copies, int n, cudaStream_t stream) {
-    if (n < 0 || (n > 0 && copies == nullptr)) return CLO_ERR_INVALID_ARG;
-    for (int i = 0; i < n; ++i)
-        if (copies[i].bytes > 0 && (copies[i].dst == nullptr || copies[i].src == nullptr))
-            return CLO_ERR_INVALID_ARG;
-    for (int i = 0; i < n; ++i) {
-        if (copies[i].bytes == 0) continue;
-        if (cudaMemcpyAsync(copies[i].dst, copies[i].src, copies[i].bytes, cudaMemcpyDefault,
-                            stream) != cudaSuccess)
-            return CLO_ERR_CUDA;
-    }
-    return CLO_OK;
 }

@@ -50,6 +50,14 @@ def test_copy_async_validates_before_issuing(L):
     assert L.clo_copy_async(ctypes.addressof(arr), -1, None) == clo.CLO_ERR_INVALID_ARG
     assert L.clo_copy_async(ctypes.addressof(arr), 2, None) == clo.CLO_ERR_INVALID_ARG
     assert L.clo_copy_async(ctypes.addressof(arr), 1, None) == clo.CLO_OK  # empty copy skipped
+    # overlapping copies in one list are refused before anything is issued
+    for a, b in [((FAKE, FAKE + 64, 64), (FAKE + 32, FAKE + 4096, 64)),   # dst / dst
+                 ((FAKE, FAKE + 64, 64), (FAKE + 4096, FAKE + 16, 32)),   # dst / src
+                 ((FAKE, FAKE + 64, 64), (FAKE + 64, FAKE + 4096, 16))]:  # src / dst
+        arr = (clo.CloCopy * 2)(clo.CloCopy(*a), clo.CloCopy(*b))
+        assert L.clo_copy_async(ctypes.addressof(arr), 2, None) == clo.CLO_ERR_INVALID_ARG
+    self_copy = (clo.CloCopy * 1)(clo.CloCopy(FAKE, FAKE + 8, 16))
+    assert L.clo_copy_async(ctypes.addressof(self_copy), 1, None) == clo.CLO_ERR_INVALID_ARG
 
 
 def test_copy_pairs_checked_in_python():

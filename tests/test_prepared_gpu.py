@@ -35,6 +35,30 @@ def test_copy_async_round_trip():
     assert torch.equal(back_b, h_b * 2.0)
 
 
+def test_copy_async_many_large_and_mixed():
+    """More copies than one launch takes (20), one of 40 MB (many CTAs), and
+    unaligned sizes (copy-engine copies) between them, in both directions."""
+    g = torch.Generator().manual_seed(6)
+    sizes = [16 * (i + 1) for i in range(19)] + [40 << 20]
+    sizes[7] = 1001  # not a multiple of 16 bytes
+    hs = [torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).pin_memory() for n in sizes]
+    ds = [torch.empty(n, dtype=torch.uint8, device=dev()) for n in sizes]
+    clo.clo_copy_async(list(zip(ds, hs)))
+    backs = [torch.empty_like(h).pin_memory() for h in hs]
+    clo.clo_copy_async(list(zip(backs, ds)))
+    torch.cuda.synchronize()
+    for h, d, b in zip(hs, ds, backs):
+        assert torch.equal(d.cpu(), h)
+        assert torch.equal(b, h)
+
+
+def test_copy_lists_may_not_overlap():
+    h = torch.zeros(64, dtype=torch.uint8).pin_memory()
+    d = torch.zeros(128, dtype=torch.uint8, device=dev())
+    with pytest.raises(clo.CloError):
+        clo.clo_copy_async([(d[:64], h), (d[32:96], h)])
+
+
 def test_copy_pairs_must_cross_the_link():
     d = torch.empty(4, device=dev())
     with pytest.raises(clo.CloError):
