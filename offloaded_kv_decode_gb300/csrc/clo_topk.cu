@@ -137,8 +137,10 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* woff, int& tota
 // One cluster of `cs` CTAs per head (cs = gridDim.x / heads); CTA r of the
 // cluster caches keys [r * slice, (r + 1) * slice) in shared memory and every
 // pass sums the cluster's histograms through distributed shared memory, so
-// every CTA takes the same digit decisions.
-__global__ void __launch_bounds__(TK_SEL_THREADS)
+// every CTA takes the same digit decisions.  Registers are held to 32 a
+// thread so two 1024-thread CTAs share an SM: at 64 a thread one CTA fills
+// the register file, and 64 heads of 4 CTAs took two waves on 152 SMs.
+__global__ void __launch_bounds__(TK_SEL_THREADS, 2)
     topk_select_kernel(const float* __restrict__ scores, int T, int k, int slice,
                        int32_t* __restrict__ idx) {
     namespace cg = cooperative_groups;
