@@ -1,0 +1,107 @@
+"""Seeded random-shape sweeps of both attention entry points against the fp64
+oracle (GPU).
+
+Each case draws its own batch, head counts (GQA 1 to 8), context, top-k size,
+number of persistent heads, Cache Buffer addressing, CTA count and, for the
+paged layout, per-request lengths (empty requests included), so the tile
+ranges, segment flushes, partial merges and ragged tails meet shapes the
+hand-picked cases do not.  The shapes are drawn by a fixed generator: a
+failure names its case and reproduces.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import offloaded_kv_decode_gb300 as clo
+from gpu_util import LSE_ATOL, assert_close, dev, scale_for
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 16
+
+
+def _hybrid_shape(i):
+    r = np.random.Generator(np.random.PCG64(1000 + i))
+    Hkv = int(r.choice([1, 2, 4, 8]))
+    G = int(r.integers(1, 9))
+    B = int(r.integers(1, 5))
+    T = int(r.integers(1, 2500))
+    k = int(r.integers(1, T + 1))
+    Np = int(r.integers(0, Hkv + 1))
+    compact = bool(r.integers(0, 2))
+    C = k if compact else T
+    num_ctas = int(r.choice([0, 0, 1, 2, 5, 17, 64]))
+    return B, Hkv * G, Hkv, T, k, Np, C, num_ctas
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_hybrid_random_shape(i):
+    B, Hq, Hkv, T, k, Np, C, num_ctas = _hybrid_shape(i)
+    r = np.random.Generator(np.random.PCG64(2000 + i))
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    q = f16(B, Hq, 128)
+    cbK, cbV = f16(B, Hkv, C, 128), f16(B, Hkv, C, 128)
+    idx = np.stack([np.stack([r.permutation(C)[:k] for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    pK, pV = f16(B, Np, T, 128), f16(B, Np, T, 128)
+    pid = r.permutation(Hkv)[:Np].astype(np.int32)
+    ref, ref_lse = oracle.get().hybrid_attn(q, cbK, cbV, idx, pK, pV, pid, scale_for())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=dev())
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev())
+    ws = torch.empty(clo.clo_hybrid_workspace_size(B, Hq, Hkv, 128, num_ctas), dtype=torch.uint8,
+                     device=dev())
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    has_cb = Np < Hkv
+    clo.clo_hybrid_decode_attn(t(q), t(cbK) if has_cb else None, t(cbV) if has_cb else None,
+                               t(idx) if has_cb else None, t(pK) if Np else None,
+                               t(pV) if Np else None, t(pid) if Np else None, out, ws, lse=lse,
+                               err_flag=err, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    case = f"B{B} Hq{Hq} Hkv{Hkv} T{T} k{k} Np{Np} C{C} ctas{num_ctas}"
+    assert int(err.item()) == 0, case
+    assert_close(out.cpu().numpy().astype(np.float64), ref, case)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) < LSE_ATOL, case
+
+
+def _paged_case(i):
+    r = np.random.Generator(np.random.PCG64(3000 + i))
+    Hkv = int(r.choice([1, 2, 8, 32]))
+    G = int(r.choice([1, 1, 4, 5, 8])) if Hkv <= 8 else 1
+    B = int(r.integers(1, 40))
+    max_ctx = int(r.integers(1, 1200))
+    ctx = r.integers(0, max_ctx + 1, size=B).astype(np.int32)
+    ctx[r.random(B) < 0.1] = 0  # idle slots
+    mb = -(-max_ctx // 16)
+    nb = B * mb + int(r.integers(0, 8))
+    bt = np.stack([r.permutation(nb)[:mb] for _ in range(B)]).astype(np.int32)
+    num_ctas = int(r.choice([0, 0, 1, 3, 19, 100]))
+    return B, Hkv * G, Hkv, nb, bt, ctx, num_ctas, r
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_paged_random_shape(i):
+    B, Hq, Hkv, nb, bt, ctx, num_ctas, r = _paged_case(i)
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    q = f16(B, Hq, 128)
+    kc, vc = f16(nb, Hkv, 16, 128), f16(nb, Hkv, 16, 128)
+    ref, ref_lse = oracle.get().paged_attn(q, kc, vc, bt, ctx, scale_for())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=dev())
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev())
+    ws = torch.empty(clo.clo_paged_workspace_size(B, Hq, Hkv, 128, num_ctas), dtype=torch.uint8,
+                     device=dev())
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    clo.clo_paged_decode_attn(t(q), t(kc), t(vc), t(bt), t(ctx), out, ws, lse=lse, err_flag=err,
+                              num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    case = f"B{B} Hq{Hq} Hkv{Hkv} blocks{nb} max_ctx{int(ctx.max())} ctas{num_ctas}"
+    assert int(err.item()) == 0, case
+    got = out.cpu().numpy().astype(np.float64)
+    assert_close(got, ref, case)
+    lse_h = lse.cpu().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.max(np.abs(lse_h[fin] - ref_lse[fin]), initial=0) < LSE_ATOL, case
+    assert np.array_equal(np.isneginf(lse_h), ~fin), case
+    assert np.all(got[ctx == 0] == 0), case
