@@ -9,10 +9,11 @@
 //
 // Two kernels:
 //   topk_score_kernel   streams every key once (HBM-bound: T * 256 bytes a
-//                       head).  A CTA owns a chunk of one head's keys; each
-//                       half-warp scores one 256-byte key row per step (16
-//                       bytes a lane, a 16-lane shuffle reduction), with 8
-//                       rows in flight per half-warp.
+//                       head).  One resident wave of CTAs, each scoring an
+//                       equal share of all heads' keys; each half-warp scores
+//                       one 256-byte key row per step (16 bytes a lane, a
+//                       16-lane shuffle reduction), with 8 rows in flight per
+//                       half-warp.
 //   topk_select_kernel  one thread-block cluster per head, each CTA holding a
 //                       slice of the head's keys (the order-preserving
 //                       integer image of the fp32 scores) in shared memory:
@@ -35,65 +36,103 @@ constexpr int TK_D = 128;
 constexpr int TK_SCORE_THREADS = 256;
 constexpr int TK_UNROLL = 8;                                      // rows in flight a half-warp
 constexpr int TK_ROWS_PER_STEP = (TK_SCORE_THREADS / 16) * TK_UNROLL;  // 128 rows a CTA step
+#ifndef CLO_TK_SCORE_CTAS_PER_SM
+#define CLO_TK_SCORE_CTAS_PER_SM 3
+#endif
+constexpr int TK_SCORE_CTAS_PER_SM = CLO_TK_SCORE_CTAS_PER_SM;  // the register cap follows
 constexpr int TK_SEL_THREADS = 1024;
 constexpr int TK_SEL_CACHE = 47 * 1024;  // keys a select CTA keeps in shared memory (188 KB)
 constexpr int TK_SEL_SLICE = 8 * 1024;   // aim for about this many keys a select CTA
 constexpr int TK_SEL_MAX_CLUSTER = 8;    // portable cluster size
 constexpr int TK_MAX_G = 8;
 
-__global__ void __launch_bounds__(TK_SCORE_THREADS)
+#ifndef CLO_TK_EVICT_FIRST
+#define CLO_TK_EVICT_FIRST 1
+#endif
+
+// A 16-byte load of a key row, read once: no L1 allocation, and in L2 evicted
+// first, so the 512 MB key stream does not push the scores the select kernel
+// reads next out of L2.
+__device__ __forceinline__ uint4 ld_key_row(const void* p, uint64_t policy) {
+    uint4 v;
+#if CLO_TK_EVICT_FIRST
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+#else
+    (void)policy;
+    v = *reinterpret_cast<const uint4*>(p);
+#endif
+    return v;
+}
+
+// The rows of all heads form one line (head-major); CTA c scores an equal
+// contiguous share of it, so one resident wave covers every key with no
+// ragged last chunk per head.  A share crosses at most a few head boundaries;
+// the group's summed query is reloaded at each.
+__global__ void __launch_bounds__(TK_SCORE_THREADS, TK_SCORE_CTAS_PER_SM)
     topk_score_kernel(const clo_half* __restrict__ q, const clo_half* __restrict__ K, int Hq,
-                      int Hkv, int G, int T, int chunk, float* __restrict__ scores) {
+                      int Hkv, int G, int T, long long rows, float* __restrict__ scores) {
     pdl_launch_dependents();
     pdl_wait();
-    const int head = blockIdx.y;  // b * Hkv + g
-    const int b = head / Hkv, g = head - b * Hkv;
     const int lane = threadIdx.x & 31, c = lane & 15, half = lane >> 4;
     const int warp = threadIdx.x >> 5;
-    // Lane c holds dims [8c, 8c + 8) of the group's summed query.
-    float qs[8];
+    const uint64_t policy = l2_evict_first_policy();
+    const long long r0 = rows * blockIdx.x / gridDim.x;
+    const long long r1 = rows * (blockIdx.x + 1) / gridDim.x;
+    if (r1 <= r0) return;
+    // Heads h_first .. h_last, from row t_first of the first to row t_last
+    // (exclusive) of the last.
+    const int h_first = static_cast<int>(r0 / T), h_last = static_cast<int>((r1 - 1) / T);
+    const int t_first = static_cast<int>(r0 - static_cast<long long>(h_first) * T);
+    const int t_last = static_cast<int>(r1 - static_cast<long long>(h_last) * T);
+    for (int head = h_first; head <= h_last; ++head) {  // head = b * Hkv + g
+        const int b = head / Hkv, g = head - b * Hkv;
+        // Lane c holds dims [8c, 8c + 8) of the group's summed query.
+        float qs[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qs[i] = 0.f;
-    const clo_half* qg = q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * TK_D + c * 8;
-    for (int j = 0; j < G; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qg + static_cast<size_t>(j) * TK_D);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int i = 0; i < 8; ++i) qs[i] = 0.f;
+        const clo_half* qg = q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * TK_D + c * 8;
+        for (int j = 0; j < G; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qg + static_cast<size_t>(j) * TK_D);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            qs[2 * i] += f.x;
-            qs[2 * i + 1] += f.y;
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                qs[2 * i] += f.x;
+                qs[2 * i + 1] += f.y;
+            }
         }
-    }
-    const clo_half* Kh = K + static_cast<size_t>(head) * T * TK_D + c * 8;
-    float* sh = scores + static_cast<size_t>(head) * T;
-    const int t0 = blockIdx.x * chunk;
-    const int t1 = min(T, t0 + chunk);
-    // The loop runs on a warp-uniform base (the shuffles below need the whole
-    // warp); half-warp h of warp w takes rows base + h + 16 u.
-    for (int base = t0 + 2 * warp; base < t1; base += TK_ROWS_PER_STEP) {
-        uint4 kv[TK_UNROLL];
+        const clo_half* Kh = K + static_cast<size_t>(head) * T * TK_D + c * 8;
+        float* sh = scores + static_cast<size_t>(head) * T;
+        const int t0 = head == h_first ? t_first : 0;
+        const int t1 = head == h_last ? t_last : T;
+        // The loop runs on a warp-uniform base (the shuffles below need the
+        // whole warp); half-warp h of warp w takes rows base + h + 16 u.
+        for (int base = t0 + 2 * warp; base < t1; base += TK_ROWS_PER_STEP) {
+            uint4 kv[TK_UNROLL];
 #pragma unroll
-        for (int u = 0; u < TK_UNROLL; ++u) {
-            const int t = base + half + u * (TK_SCORE_THREADS / 16);
-            if (t < t1) kv[u] = *reinterpret_cast<const uint4*>(Kh + static_cast<size_t>(t) * TK_D);
-        }
-#pragma unroll
-        for (int u = 0; u < TK_UNROLL; ++u) {
-            const int t = base + half + u * (TK_SCORE_THREADS / 16);
-            float acc = 0.f;
-            if (t < t1) {
-                const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-                    acc = fmaf(qs[2 * i], f.x, acc);
-                    acc = fmaf(qs[2 * i + 1], f.y, acc);
-                }
+            for (int u = 0; u < TK_UNROLL; ++u) {
+                const int t = base + half + u * (TK_SCORE_THREADS / 16);
+                if (t < t1) kv[u] = ld_key_row(Kh + static_cast<size_t>(t) * TK_D, policy);
             }
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, off);
-            if (c == 0 && t < t1) sh[t] = acc;
+            for (int u = 0; u < TK_UNROLL; ++u) {
+                const int t = base + half + u * (TK_SCORE_THREADS / 16);
+                float acc = 0.f;
+                if (t < t1) {
+                    const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                        acc = fmaf(qs[2 * i], f.x, acc);
+                        acc = fmaf(qs[2 * i + 1], f.y, acc);
+                    }
+                }
+#pragma unroll
+                for (int off = 8; off >= 1; off >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, off);
+                if (c == 0 && t < t1) sh[t] = acc;
+            }
         }
     }
 }
@@ -348,16 +387,15 @@ extern "C" clo_status clo_topk_retrieve(const clo_half* q, const clo_half* K, in
     const int heads = B * Hkv;
     const int sms = device_sm_count();
     if (sms <= 0) return CLO_ERR_CUDA;
-    // About 8 score CTAs per SM in total, each a multiple of one CTA step.
-    long long chunks = (static_cast<long long>(sms) * 8 + heads - 1) / heads;
-    long long chunk = (T + chunks - 1) / chunks;
-    chunk = std::max<long long>(TK_ROWS_PER_STEP, (chunk + TK_ROWS_PER_STEP - 1) / TK_ROWS_PER_STEP * TK_ROWS_PER_STEP);
-    chunks = (T + chunk - 1) / chunk;
+    // One resident wave of score CTAs, each with at least one CTA step of rows.
+    const long long rows = static_cast<long long>(heads) * T;
+    long long score_ctas = static_cast<long long>(sms) * TK_SCORE_CTAS_PER_SM;
+    score_ctas = std::max(1ll, std::min(score_ctas, rows / TK_ROWS_PER_STEP));
     if (opts != nullptr && opts->ev_begin != nullptr && !record_event(opts->ev_begin, stream))
         return CLO_ERR_CUDA;
-    if (launch_pdl(topk_score_kernel, dim3(static_cast<unsigned>(chunks), heads),
-                   dim3(TK_SCORE_THREADS), 0, stream, q, K, Hq, Hkv, G, T,
-                   static_cast<int>(chunk), scores) != cudaSuccess)
+    if (launch_pdl(topk_score_kernel, dim3(static_cast<unsigned>(score_ctas)),
+                   dim3(TK_SCORE_THREADS), 0, stream, q, K, Hq, Hkv, G, T, rows, scores) !=
+        cudaSuccess)
         return CLO_ERR_CUDA;
     if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
