@@ -48,9 +48,16 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ void st_row(void* p, const uint4& v) {
-    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
+// A 16-byte store of a Cache Buffer row, evicted from L2 first.  The fill of
+// a layer runs while the layer before it computes (the lookup is one layer
+// ahead), so the hundreds of MB that attention streams would evict the rows
+// before their own attention reads them anyway; the hint keeps them from
+// pushing out what the kernels around the fill reuse.  (On the B8 32K
+// full-miss fill from HBM it measured 35.0 -> 34.6 us; the same hint on the
+// loads measured 35.8 us.)
+__device__ __forceinline__ void st_row(void* p, const uint4& v, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
                  : "memory");
 }
 
@@ -67,6 +74,7 @@ __global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM) fill_kernel(co
     const int half = lane >> 4, chunk = lane & 15;
     const long long warp0 = static_cast<long long>(blockIdx.x) * FILL_WARPS + (threadIdx.x >> 5);
     const long long nwarps = static_cast<long long>(gridDim.x) * FILL_WARPS;
+    const uint64_t policy = l2_evict_first_policy();
     bool bad = false;
     for (long long base = warp0 * FILL_ROWS; base < rows; base += nwarps * FILL_ROWS) {
         // Lane i < 16 resolves row base + i: its head entry, token and slot.
@@ -106,8 +114,8 @@ __global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM) fill_kernel(co
 #pragma unroll
         for (int u = 0; u < FILL_ROWS / 2; ++u) {
             if (dst[u] >= 0) {
-                st_row(p.cbK + dst[u] * FILL_D + chunk * 8, vk[u]);
-                st_row(p.cbV + dst[u] * FILL_D + chunk * 8, vv[u]);
+                st_row(p.cbK + dst[u] * FILL_D + chunk * 8, vk[u], policy);
+                st_row(p.cbV + dst[u] * FILL_D + chunk * 8, vv[u], policy);
             }
         }
     }
