@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(TK_SEL_THREADS, 2)
     pdl_wait();
     constexpr int kWarps = TK_SEL_THREADS / 32;
     __shared__ int hist[kWarps][256];  // one histogram per warp (no contention between warps)
-    __shared__ int total[256];         // this CTA's counts, read by the whole cluster
+    __shared__ int total[2][256];      // this CTA's counts, read by the whole cluster (by pass parity)
     __shared__ int gtotal[256];
     __shared__ int wsum[kWarps];
     __shared__ int woff[kWarps + 1];
@@ -221,8 +221,11 @@ __global__ void __launch_bounds__(TK_SEL_THREADS, 2)
         sel_need = k;
     }
     uint32_t mask = 0u;
-    int last_digit = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    int last_digit = 0, par = 0;
+    // Pass p writes total[p & 1].  The other CTAs read it between this pass's
+    // cluster barrier and the next one, and pass p + 2 writes it only after
+    // that next barrier, so one cluster barrier a pass is enough.
+    for (int shift = 24; shift >= 0; shift -= 8, par ^= 1) {
         for (int i = lane; i < 256; i += 32) hist[warp][i] = 0;
         __syncthreads();
         const uint32_t prefix = sel_prefix;
@@ -243,12 +246,12 @@ __global__ void __launch_bounds__(TK_SEL_THREADS, 2)
         for (int i = threadIdx.x; i < 256; i += TK_SEL_THREADS) {
             int c = 0;
             for (int w = 0; w < kWarps; ++w) c += hist[w][i];
-            total[i] = c;
+            total[par][i] = c;
         }
         cluster.sync();  // every CTA's counts are final
         for (int i = threadIdx.x; i < 256; i += TK_SEL_THREADS) {
             int c = 0;
-            for (int r = 0; r < cs; ++r) c += cluster.map_shared_rank(total, r)[i];
+            for (int r = 0; r < cs; ++r) c += cluster.map_shared_rank(&total[par][0], r)[i];
             gtotal[i] = c;
         }
         __syncthreads();
@@ -285,8 +288,8 @@ __global__ void __launch_bounds__(TK_SEL_THREADS, 2)
         mask |= 255u << shift;
         __syncthreads();
         last_digit = static_cast<int>((sel_prefix >> shift) & 255u);
-        cluster.sync();  // nobody reads this pass's counts any more
     }
+    const int last_par = par ^ 1;  // the buffer of the last pass
     // kth = the k-th largest key of the row; the row keeps every larger key
     // and the first `ties` keys equal to it, in token order.
     const uint32_t kth = sel_prefix;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(TK_SEL_THREADS, 2)
     (void)block_scan(above, wsum, woff, above_total);
     if (threadIdx.x == 0) {
         counts[0] = above_total;
-        counts[1] = total[last_digit];  // the last pass counted exactly the keys equal to kth
+        counts[1] = total[last_par][last_digit];  // the last pass counted exactly the keys equal to kth
     }
     cluster.sync();
     int out_base = 0, ties_before = 0;
