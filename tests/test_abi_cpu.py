@@ -198,3 +198,34 @@ def test_topk_rejects(L):
     assert topk(wsb=10) == clo.CLO_ERR_WORKSPACE
     assert topk(k=0) == clo.CLO_OK and topk(B=0) == clo.CLO_OK
     assert clo.clo_topk_workspace_size(2, 8, 100) == 2 * 8 * 100 * 4
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """clo.h compiles as C99 and a C program links against libclo.so and calls
+    it through the header's declarations alone (no torch, no GPU work)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "use_clo.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <string.h>\n#include "clo.h"\n'
+        "int main(void) {\n"
+        "    if (clo_version() < 10000) return 1;\n"
+        '    if (strcmp(clo_status_string(CLO_ERR_WORKSPACE), "CLO_ERR_WORKSPACE") != 0) return 2;\n'
+        "    if (clo_check_error_flag(CLO_FLAG_BAD_PERSIST) != CLO_ERR_BAD_INDEX) return 3;\n"
+        "    if (clo_copy_async(NULL, -1, 0) != CLO_ERR_INVALID_ARG) return 4;\n"
+        "    if (clo_hybrid_workspace_size(1, 32, 8, 128, 152) == 0) return 5;\n"
+        '    printf("ok\\n");\n'
+        "    return 0;\n}\n")
+    exe = tmp_path / "use_clo"
+    libdir = os.path.dirname(clo.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", libdir, "-lclo",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
