@@ -126,6 +126,7 @@ def test_hybrid_rejects(L):
     assert _hybrid(L, scale=float("nan")) == clo.CLO_ERR_INVALID_ARG
     assert _hybrid(L, d=96) == clo.CLO_ERR_UNSUPPORTED
     assert _hybrid(L, Hq=80, Hkv=8) == clo.CLO_ERR_UNSUPPORTED  # G = 10
+    assert _hybrid(L, Hq=65, Hkv=65) == clo.CLO_ERR_UNSUPPORTED  # more KV heads than the limit (64)
     assert _hybrid(L, B=0) == clo.CLO_OK                        # empty batch: nothing to do
     # All heads persistent: no Cache Buffer pointers needed, k may be 0.
     assert L.clo_hybrid_decode_attn(FAKE, None, None, None, 0, 0, FAKE, FAKE, FAKE, 8, 5, 0,

@@ -105,3 +105,61 @@ def test_paged_random_shape(i):
     assert np.max(np.abs(lse_h[fin] - ref_lse[fin]), initial=0) < LSE_ATOL, case
     assert np.array_equal(np.isneginf(lse_h), ~fin), case
     assert np.all(got[ctx == 0] == 0), case
+
+
+def test_hybrid_at_the_head_limits():
+    """The largest query group (G = 8) over the most KV heads a call takes (64),
+    with persistent and Cache Buffer heads, against the oracle."""
+    r = np.random.Generator(np.random.PCG64(4001))
+    B, Hkv, G, T, k, Np = 2, 64, 8, 90, 23, 13
+    Hq = Hkv * G
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    q = f16(B, Hq, 128)
+    cbK, cbV = f16(B, Hkv, T, 128), f16(B, Hkv, T, 128)
+    idx = np.stack([np.stack([r.permutation(T)[:k] for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    pK, pV = f16(B, Np, T, 128), f16(B, Np, T, 128)
+    pid = r.permutation(Hkv)[:Np].astype(np.int32)
+    ref, ref_lse = oracle.get().hybrid_attn(q, cbK, cbV, idx, pK, pV, pid, scale_for())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=dev())
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev())
+    ws = torch.empty(clo.clo_hybrid_workspace_size(B, Hq, Hkv), dtype=torch.uint8, device=dev())
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    clo.clo_hybrid_decode_attn(t(q), t(cbK), t(cbV), t(idx), t(pK), t(pV), t(pid), out, ws,
+                               lse=lse, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(out.cpu().numpy().astype(np.float64), ref, "64 KV heads, G = 8")
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) < LSE_ATOL
+
+
+def test_paged_at_the_request_limit():
+    """The most requests a paged call takes (4096) at G = 8, short contexts with
+    idle slots, against the oracle."""
+    r = np.random.Generator(np.random.PCG64(4002))
+    B, Hkv, G = 4096, 1, 8
+    Hq = Hkv * G
+    ctx = r.integers(0, 41, size=B).astype(np.int32)
+    mb = 3
+    nb = B * mb
+    bt = r.permutation(nb).reshape(B, mb).astype(np.int32)
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    q = f16(B, Hq, 128)
+    kc, vc = f16(nb, Hkv, 16, 128), f16(nb, Hkv, 16, 128)
+    ref, ref_lse = oracle.get().paged_attn(q, kc, vc, bt, ctx, scale_for())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=dev())
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev())
+    ws = torch.empty(clo.clo_paged_workspace_size(B, Hq, Hkv), dtype=torch.uint8, device=dev())
+    err = torch.zeros(1, dtype=torch.int32, device=dev())
+    clo.clo_paged_decode_attn(t(q), t(kc), t(vc), t(bt), t(ctx), out, ws, lse=lse, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    assert_close(got, ref, "4096 requests, G = 8")
+    lse_h = lse.cpu().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.max(np.abs(lse_h[fin] - ref_lse[fin]), initial=0) < LSE_ATOL
+    assert np.array_equal(np.isneginf(lse_h), ~fin)
+    assert np.all(got[ctx == 0] == 0)
