@@ -97,12 +97,12 @@ typedef struct clo_copy {
  * call instead of one per buffer.  The pages have no counterpart: it is the
  * host-buffer edge of this library, and nothing in it computes.
  *  - Copies between memory the GPU can address (device or managed memory,
- *    pinned host memory) that are 16-byte aligned and a multiple of 16 bytes
- *    long are made by a libclo kernel, up to 16 of them a launch; the SMs read
- *    and write host memory over the host link.  That kernel chains with the
- *    libclo kernels before and after it like they chain with each other.  Any
- *    other copy is one cudaMemcpyAsync (pageable host memory makes that wait
- *    for the copy).
+ *    pinned host memory) are made by a libclo kernel, up to 16 of them a
+ *    launch, when both ends are 16-byte aligned (any length) or the copy is at
+ *    most 64 KiB; the SMs read and write host memory over the host link.  That
+ *    kernel chains with the libclo kernels before and after it like they chain
+ *    with each other.  Any other copy is one cudaMemcpyAsync (pageable host
+ *    memory makes that wait for the copy).
  *  - The copies of one call may run at the same time: a list in which one
  *    copy writes bytes that another reads or writes (or a copy onto itself)
  *    gives CLO_ERR_INVALID_ARG.  Calls are ordered on the stream as usual.

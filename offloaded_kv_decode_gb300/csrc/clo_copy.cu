@@ -3,15 +3,16 @@
 // the host.  The pages have no counterpart; nothing here computes.
 //
 // Copies whose two sides the GPU can address (device or managed memory, or
-// pinned host memory through its mapped device address), 16-byte aligned
-// and a multiple of 16 bytes long, are made by one kernel launch per run of
-// up to COPY_MAX such copies: the SMs read and write host memory over the
-// host link themselves.  That launch takes part in programmatic dependent
-// launch like every other libclo kernel, so it chains with the kernels
-// around it; a copy-engine copy between two kernels would make the second
-// wait for the first to drain and for the copy before it could start.  Any
-// other copy goes to cudaMemcpyAsync.  The copies of one call may run at the
-// same time, so the call refuses lists whose copies overlap.
+// pinned host memory through its mapped device address) are made by one
+// kernel launch per run of up to COPY_MAX such copies: the SMs read and write
+// host memory over the host link themselves.  Copies with both ends 16-byte
+// aligned move 16 bytes a thread, any others (up to COPY_SMALL bytes) a byte
+// a thread.  That launch takes part in programmatic dependent launch like
+// every other libclo kernel, so it chains with the kernels around it; a
+// copy-engine copy between two kernels would make the second wait for the
+// first to drain and for the copy before it could start.  Any other copy
+// goes to cudaMemcpyAsync.  The copies of one call may run at the same time,
+// so the call refuses lists whose copies overlap.
 #include <algorithm>
 
 #include "clo_device.cuh"
@@ -22,36 +23,47 @@ constexpr int COPY_MAX = 16;       // copies a launch
 constexpr int COPY_THREADS = 256;
 constexpr int COPY_UNROLL = 4;     // independent 16-byte loads a thread keeps in flight
 constexpr int COPY_CTAS_PER_SM = 8;
+constexpr size_t COPY_SMALL = 64 * 1024;  // largest copy the kernel makes a byte at a time
 
 struct CopyList {
-    uint4* dst[COPY_MAX];
-    const uint4* src[COPY_MAX];
-    long long n16[COPY_MAX];  // 16-byte units
+    char* dst[COPY_MAX];
+    const char* src[COPY_MAX];
+    long long bytes[COPY_MAX];
 };
 
-// Copy blockIdx.y of the list; the CTAs along x stride over its units.
+__device__ __forceinline__ bool both_aligned16(const void* a, const void* b) {
+    return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
+}
+
+// Copy blockIdx.y of the list; the CTAs along x stride over it: 16-byte
+// units when both ends are 16-byte aligned, then the bytes past the last
+// whole unit (all of them otherwise).
 __global__ void __launch_bounds__(COPY_THREADS) copy_kernel(const CopyList c) {
     pdl_launch_dependents();
     pdl_wait();  // the source may come from the kernel before
     const int i = blockIdx.y;
-    const uint4* __restrict__ src = c.src[i];
-    uint4* __restrict__ dst = c.dst[i];
-    const long long n = c.n16[i];
+    const char* __restrict__ src = c.src[i];
+    char* __restrict__ dst = c.dst[i];
+    const long long bytes = c.bytes[i];
+    const long long n = both_aligned16(dst, src) ? bytes / 16 : 0;
+    const uint4* __restrict__ src16 = reinterpret_cast<const uint4*>(src);
+    uint4* __restrict__ dst16 = reinterpret_cast<uint4*>(dst);
     const long long stride = static_cast<long long>(gridDim.x) * COPY_THREADS;
-    for (long long base = static_cast<long long>(blockIdx.x) * COPY_THREADS + threadIdx.x;
-         base < n; base += stride * COPY_UNROLL) {
+    const long long first = static_cast<long long>(blockIdx.x) * COPY_THREADS + threadIdx.x;
+    for (long long base = first; base < n; base += stride * COPY_UNROLL) {
         uint4 v[COPY_UNROLL];
 #pragma unroll
         for (int u = 0; u < COPY_UNROLL; ++u) {
             const long long j = base + u * stride;
-            if (j < n) v[u] = src[j];
+            if (j < n) v[u] = src16[j];
         }
 #pragma unroll
         for (int u = 0; u < COPY_UNROLL; ++u) {
             const long long j = base + u * stride;
-            if (j < n) dst[j] = v[u];
+            if (j < n) dst16[j] = v[u];
         }
     }
+    for (long long b = n * 16 + first; b < bytes; b += stride) dst[b] = src[b];
 }
 
 // The address the GPU reaches p through, or nullptr if it cannot (pageable
@@ -71,10 +83,12 @@ static void* device_address(const void* p) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static clo_status launch_copies(const CopyList& c, int n, long long most16, cudaStream_t stream) {
+// most: the largest copy of the batch in work units (16-byte units, or bytes
+// for a byte copy).
+static clo_status launch_copies(const CopyList& c, int n, long long most, cudaStream_t stream) {
     const int sms = device_sm_count();
     if (sms <= 0) return CLO_ERR_CUDA;
-    long long gx = (most16 + static_cast<long long>(COPY_THREADS) * COPY_UNROLL - 1) /
+    long long gx = (most + static_cast<long long>(COPY_THREADS) * COPY_UNROLL - 1) /
                    (static_cast<long long>(COPY_THREADS) * COPY_UNROLL);
     const long long cap = static_cast<long long>(sms) * COPY_CTAS_PER_SM / n;
     if (gx > cap) gx = cap;
@@ -114,36 +128,36 @@ extern "C" clo_status clo_copy_async(const clo_copy* copies, int n, cudaStream_t
     }
     CopyList batch{};
     int nb = 0;
-    long long most16 = 0;
+    long long most = 0;
     for (int i = 0; i < n; ++i) {
         const clo_copy& cp = copies[i];
         if (cp.bytes == 0) continue;
         void* d = device_address(cp.dst);
         const void* s = device_address(cp.src);
-        const bool by_kernel = d != nullptr && s != nullptr && aligned16(d) && aligned16(s) &&
-                               cp.bytes % 16 == 0;
+        const bool vec = d != nullptr && s != nullptr && aligned16(d) && aligned16(s);
+        const bool by_kernel = d != nullptr && s != nullptr && (vec || cp.bytes <= COPY_SMALL);
         if (by_kernel) {
-            batch.dst[nb] = static_cast<uint4*>(d);
-            batch.src[nb] = static_cast<const uint4*>(s);
-            batch.n16[nb] = static_cast<long long>(cp.bytes / 16);
-            most16 = std::max(most16, batch.n16[nb]);
+            batch.dst[nb] = static_cast<char*>(d);
+            batch.src[nb] = static_cast<const char*>(s);
+            batch.bytes[nb] = static_cast<long long>(cp.bytes);
+            most = std::max(most, static_cast<long long>(vec ? (cp.bytes + 15) / 16 : cp.bytes));
             if (++nb == COPY_MAX) {
-                const clo_status st = launch_copies(batch, nb, most16, stream);
+                const clo_status st = launch_copies(batch, nb, most, stream);
                 if (st != CLO_OK) return st;
                 nb = 0;
-                most16 = 0;
+                most = 0;
             }
             continue;
         }
         if (nb > 0) {  // keep the list order
-            const clo_status st = launch_copies(batch, nb, most16, stream);
+            const clo_status st = launch_copies(batch, nb, most, stream);
             if (st != CLO_OK) return st;
             nb = 0;
-            most16 = 0;
+            most = 0;
         }
         if (cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDefault, stream) != cudaSuccess)
             return CLO_ERR_CUDA;
     }
-    if (nb > 0) return launch_copies(batch, nb, most16, stream);
+    if (nb > 0) return launch_copies(batch, nb, most, stream);
     return CLO_OK;
 }

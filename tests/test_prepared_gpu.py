@@ -52,6 +52,26 @@ def test_copy_async_many_large_and_mixed():
         assert torch.equal(b, h)
 
 
+def test_copy_async_unaligned_ends():
+    """Ends off the 16-byte grid: small copies go byte by byte through the
+    kernel, a large one (past 64 KiB) through the copy engine; both directions."""
+    g = torch.Generator().manual_seed(7)
+    sizes = [1, 4, 13, 4099, 70000]
+    hs = [torch.randint(0, 256, (n + 3,), dtype=torch.uint8, generator=g).pin_memory()
+          for n in sizes]
+    ds = [torch.zeros(n + 5, dtype=torch.uint8, device=dev()) for n in sizes]
+    clo.clo_copy_async([(d[1:1 + n], h[3:3 + n]) for d, h, n in zip(ds, hs, sizes)])
+    backs = [torch.zeros(n + 2, dtype=torch.uint8).pin_memory() for n in sizes]
+    clo.clo_copy_async([(b[2:2 + n], d[1:1 + n]) for b, d, n in zip(backs, ds, sizes)])
+    torch.cuda.synchronize()
+    for h, d, b, n in zip(hs, ds, backs, sizes):
+        dc = d.cpu()
+        assert torch.equal(dc[1:1 + n], h[3:3 + n])
+        assert dc[0] == 0 and torch.all(dc[1 + n:] == 0)  # nothing written outside the copy
+        assert torch.equal(b[2:2 + n], h[3:3 + n])
+        assert torch.all(b[:2] == 0)
+
+
 def test_copy_lists_may_not_overlap():
     h = torch.zeros(64, dtype=torch.uint8).pin_memory()
     d = torch.zeros(128, dtype=torch.uint8, device=dev())
