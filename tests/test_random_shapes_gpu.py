@@ -163,3 +163,35 @@ def test_paged_at_the_request_limit():
     assert np.max(np.abs(lse_h[fin] - ref_lse[fin]), initial=0) < LSE_ATOL
     assert np.array_equal(np.isneginf(lse_h), ~fin)
     assert np.all(got[ctx == 0] == 0)
+
+
+@pytest.mark.parametrize("gain", [8.0, 40.0])
+def test_peaked_softmax(gain):
+    """Queries scaled so the scores spread over tens to hundreds of nats: one
+    or a few tokens carry the softmax, the running maximum moves late in the
+    stream, and the split partials differ in scale by far more than fp32's
+    range (their merge must rescale, not add)."""
+    r = np.random.Generator(np.random.PCG64(5000 + int(gain)))
+    B, Hkv, G, T, k, Np = 2, 8, 4, 3000, 300, 2
+    Hq = Hkv * G
+    q = (r.standard_normal((B, Hq, 128)) * gain).astype(np.float16)
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    cbK, cbV = f16(B, Hkv, T, 128), f16(B, Hkv, T, 128)
+    idx = np.stack([np.stack([r.permutation(T)[:k] for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    pK, pV = f16(B, Np, T, 128), f16(B, Np, T, 128)
+    pid = r.permutation(Hkv)[:Np].astype(np.int32)
+    ref, ref_lse = oracle.get().hybrid_attn(q, cbK, cbV, idx, pK, pV, pid, scale_for())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    for num_ctas in (0, 7):
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=dev())
+        lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev())
+        ws = torch.empty(clo.clo_hybrid_workspace_size(B, Hq, Hkv, 128, num_ctas),
+                         dtype=torch.uint8, device=dev())
+        clo.clo_hybrid_decode_attn(t(q), t(cbK), t(cbV), t(idx), t(pK), t(pV), t(pid), out, ws,
+                                   lse=lse, num_ctas=num_ctas)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy().astype(np.float64), ref, f"gain {gain}, {num_ctas} CTAs")
+        # lse grows with the gain; hold it to the same relative precision
+        err = np.abs(lse.cpu().numpy() - ref_lse)
+        assert np.all(err < LSE_ATOL * np.maximum(1.0, np.abs(ref_lse))), f"gain {gain}"
