@@ -68,6 +68,9 @@ def compare(q, K, k):
     (1, 16, 4, 130, 130),     # everything
     (2, 32, 8, 90, 9),        # less than one CTA step of keys
     (1, 8, 2, 60000, 6000),   # more keys than the select kernel keeps in shared memory
+    (1, 4, 1, 8193, 820),     # one key past a one-CTA slice: a cluster of 2
+    (2, 8, 1, 100000, 1000),  # a cluster of 8, slices of 12500 keys
+    (1, 4, 1, 300000, 30000), # a cluster of 8 near the largest slice (37500 keys)
 ])
 def test_topk_vs_oracle(B, Hq, Hkv, T, k):
     q, K = _gen(B * 1000 + T, B, Hq, Hkv, T)
