@@ -105,7 +105,8 @@ typedef struct clo_copy {
  *    memory makes that wait for the copy).
  *  - The copies of one call may run at the same time: a list in which one
  *    copy writes bytes that another reads or writes (or a copy onto itself)
- *    gives CLO_ERR_INVALID_ARG.  Calls are ordered on the stream as usual.
+ *    gives CLO_ERR_INVALID_ARG (checked on the host in O(n log n)).  Calls are
+ *    ordered on the stream as usual.
  *  - The caller keeps every buffer alive and unchanged until the stream
  *    reaches the copy.
  *  - Copies with bytes == 0 are skipped.  n < 0, copies == NULL with n > 0,

@@ -14,6 +14,7 @@
 // goes to cudaMemcpyAsync.  The copies of one call may run at the same time,
 // so the call refuses lists whose copies overlap.
 #include <algorithm>
+#include <vector>
 
 #include "clo_device.cuh"
 
@@ -109,22 +110,36 @@ extern "C" clo_status clo_copy_async(const clo_copy* copies, int n, cudaStream_t
         if (copies[i].bytes > 0 && (copies[i].dst == nullptr || copies[i].src == nullptr))
             return CLO_ERR_INVALID_ARG;
     // Copies of one call may run at the same time: none may write bytes that
-    // another one reads or writes (all pointers share the unified address space).
-    const auto overlap = [](const void* a, const void* b, size_t na, size_t nb) {
-        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-        return x < y + nb && y < x + na;
+    // another one (or itself) reads or writes; reads may overlap reads.  The
+    // byte ranges (all pointers share the unified address space) are swept in
+    // address order: a range that starts below the end of an earlier write,
+    // or a write that starts below the end of any earlier range, overlaps it.
+    struct Range {
+        uintptr_t lo, hi;
+        bool write;
     };
+    std::vector<Range> ranges;
+    try {
+        ranges.reserve(2 * static_cast<size_t>(n));
+    } catch (...) {  // no exception leaves the library
+        return CLO_ERR_UNSUPPORTED;
+    }
     for (int i = 0; i < n; ++i) {
-        const clo_copy& a = copies[i];
-        if (a.bytes == 0) continue;
-        if (overlap(a.dst, a.src, a.bytes, a.bytes)) return CLO_ERR_INVALID_ARG;
-        for (int j = i + 1; j < n; ++j) {
-            const clo_copy& b = copies[j];
-            if (b.bytes == 0) continue;
-            if (overlap(a.dst, b.dst, a.bytes, b.bytes) || overlap(a.dst, b.src, a.bytes, b.bytes) ||
-                overlap(a.src, b.dst, a.bytes, b.bytes))
-                return CLO_ERR_INVALID_ARG;
-        }
+        const clo_copy& cp = copies[i];
+        if (cp.bytes == 0) continue;
+        const uintptr_t d = reinterpret_cast<uintptr_t>(cp.dst);
+        const uintptr_t r = reinterpret_cast<uintptr_t>(cp.src);
+        if (d + cp.bytes < d || r + cp.bytes < r) return CLO_ERR_INVALID_ARG;  // wraps around
+        ranges.push_back({d, d + cp.bytes, true});
+        ranges.push_back({r, r + cp.bytes, false});
+    }
+    std::sort(ranges.begin(), ranges.end(),
+              [](const Range& a, const Range& b) { return a.lo < b.lo; });
+    uintptr_t end_any = 0, end_write = 0;
+    for (const Range& g : ranges) {
+        if (g.lo < end_write || (g.write && g.lo < end_any)) return CLO_ERR_INVALID_ARG;
+        end_any = std::max(end_any, g.hi);
+        if (g.write) end_write = std::max(end_write, g.hi);
     }
     CopyList batch{};
     int nb = 0;

@@ -58,6 +58,12 @@ def test_copy_async_validates_before_issuing(L):
         assert L.clo_copy_async(ctypes.addressof(arr), 2, None) == clo.CLO_ERR_INVALID_ARG
     self_copy = (clo.CloCopy * 1)(clo.CloCopy(FAKE, FAKE + 8, 16))
     assert L.clo_copy_async(ctypes.addressof(self_copy), 1, None) == clo.CLO_ERR_INVALID_ARG
+    # a long list whose only conflict is between its first and last copy
+    n = 3000
+    arr = (clo.CloCopy * n)(*[clo.CloCopy(FAKE + 64 * i, FAKE + (1 << 24) + 64 * i, 32)
+                              for i in range(n)])
+    arr[n - 1] = clo.CloCopy(FAKE + (1 << 24) + 16, FAKE + (1 << 25), 8)  # writes copy 0's source
+    assert L.clo_copy_async(ctypes.addressof(arr), n, None) == clo.CLO_ERR_INVALID_ARG
 
 
 def test_copy_pairs_checked_in_python():

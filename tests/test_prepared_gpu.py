@@ -77,6 +77,11 @@ def test_copy_lists_may_not_overlap():
     d = torch.zeros(128, dtype=torch.uint8, device=dev())
     with pytest.raises(clo.CloError):
         clo.clo_copy_async([(d[:64], h), (d[32:96], h)])
+    # reads may overlap reads: one source into two places
+    h[:] = torch.arange(64, dtype=torch.uint8)
+    clo.clo_copy_async([(d[:64], h), (d[64:], h)])
+    torch.cuda.synchronize()
+    assert torch.equal(d[:64].cpu(), h) and torch.equal(d[64:].cpu(), h)
 
 
 def test_copy_pairs_must_cross_the_link():
