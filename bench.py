@@ -88,8 +88,36 @@ def paged_bytes(pc, ctx: np.ndarray) -> int:
 
 # ---------------------------------------------------------------- workloads (GPU)
 
+class E2ECopies:
+    """The host-buffer copies of an end-to-end loop over fixed buffers: each
+    step copies its inputs in; the previous step's results go out in the same
+    clo_copy_async call (they are adjacent on the stream and touch disjoint
+    memory), and finish() copies the last step's results out."""
+
+    def __init__(self, clo, ins, outs):
+        self.only_in = clo.prepare_copies(ins)
+        self.out_in = clo.prepare_copies(list(outs) + list(ins))
+        self.only_out = clo.prepare_copies(outs)
+        self.pending = False
+
+    def step_in(self):
+        (self.out_in if self.pending else self.only_in)()
+        self.pending = True
+
+    def finish(self):
+        if self.pending:
+            self.only_out()
+            self.pending = False
+
+
+PIPELINED_E2E = ("public API: prepared calls and clo_copy_async to and from pinned host buffers, "
+                 "issued from Python each step; a step's result copy shares one call with the next "
+                 "step's input copy, the last step's results are copied out inside the timed region")
+
+
 class HybridWorkload:
     kind = "hybrid"
+    e2e_path = PIPELINED_E2E
 
     def __init__(self, cfg, dev, rank: int, replicas: int = 0, schedule: str = "fused"):
         import torch
@@ -245,15 +273,16 @@ class HybridWorkload:
     # public API on buffers fixed for the run: the calls and the copy lists
     # are prepared once (checked and marshalled) and re-issued each step, and
     # the copies are made by the library (clo_copy_async) from and to pinned
-    # host memory.
+    # host memory.  A step's result copy and the next step's query copy are
+    # next to each other on the stream and touch disjoint memory, so they go
+    # out as one call (one copy launch); e2e_finish copies the last step out.
     def e2e_setup(self):
         clo, cfg = self.clo, self.cfg
         self.h_q = self.q_all.cpu().pin_memory()
         self.h_io = self.io_all.cpu().pin_memory()
         self.e2e_h2d = self.q_all.numel() * HALF
         self.e2e_d2h = self.io_all.numel()
-        self.e2e_in = clo.prepare_copies([(self.q_all, self.h_q)])
-        self.e2e_out = clo.prepare_copies([(self.h_io, self.io_all)])
+        self.e2e_pipe = E2ECopies(clo, [(self.q_all, self.h_q)], [(self.h_io, self.io_all)])
         self.e2e_tau = clo.prepare_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
         self.e2e_layer = []
         for j, it in enumerate(self.inst):
@@ -277,12 +306,14 @@ class HybridWorkload:
             self.e2e_layer.append(calls)
 
     def e2e_step(self, step: int):
-        self.e2e_in()
+        self.e2e_pipe.step_in()
         self.e2e_tau()
         for l in range(self.L):
             for call in self.e2e_layer[(step * self.L + l) % self.n_inst]:
                 call()
-        self.e2e_out()
+
+    def e2e_finish(self):
+        self.e2e_pipe.finish()
 
     def lookup_stats(self, reps: int = 50) -> dict:
         """The lookup on its own, after the timed region: hit rate and
@@ -349,6 +380,7 @@ class HybridWorkload:
 
 class PagedWorkload:
     kind = "paged"
+    e2e_path = PIPELINED_E2E
 
     def __init__(self, pc, dev, rank: int):
         import torch
@@ -386,15 +418,16 @@ class PagedWorkload:
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
         self.e2e_h2d = self.q.numel() * HALF
         self.e2e_d2h = self.out.numel() * HALF
-        self.e2e_calls = (clo.prepare_copies([(self.q, self.h_q)]),
-                          clo.prepare_paged_decode_attn(self.q, self.kc, self.vc, self.bt,
-                                                        self.ctx, self.out, self.ws,
-                                                        err_flag=self.err),
-                          clo.prepare_copies([(self.h_out, self.out)]))
+        self.e2e_pipe = E2ECopies(clo, [(self.q, self.h_q)], [(self.h_out, self.out)])
+        self.e2e_call = clo.prepare_paged_decode_attn(self.q, self.kc, self.vc, self.bt, self.ctx,
+                                                      self.out, self.ws, err_flag=self.err)
 
     def e2e_step(self, step: int):
-        for call in self.e2e_calls:
-            call()
+        self.e2e_pipe.step_in()
+        self.e2e_call()
+
+    def e2e_finish(self):
+        self.e2e_pipe.finish()
 
     def config(self) -> dict:
         c = self.cfg
@@ -957,8 +990,10 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         W.e2e_setup()
+        finish = getattr(W, "e2e_finish", lambda: None)
         for i in range(args.warmup):
             W.e2e_step(i)
+        finish()
         torch.cuda.synchronize(dev)
         barrier(pg)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -966,6 +1001,7 @@ def run_ours(args):
         e0.record(stream)
         for i in range(K):
             W.e2e_step(i)
+        finish()  # the last step's results out, inside the timed region
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(pg)
@@ -973,8 +1009,8 @@ def run_ours(args):
         e2e = {"value": aggregate_value(step_bytes, world, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": W.e2e_h2d, "d2h_bytes_per_step": W.e2e_d2h,
                "ms_per_step": e2e_ms,
-               "path": "public API: prepared calls and clo_copy_async to and from pinned "
-                       "host buffers, issued from Python each step"}
+               "path": getattr(W, "e2e_path", "public API: prepared calls and clo_copy_async "
+                               "to and from pinned host buffers, issued from Python each step")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
