@@ -17,11 +17,12 @@ variant) before timing.  Every workload cycles over physical buffer sets so
 that the bytes between two reads of the same address exceed the 129 MB L2
 (no L2 flush is needed).
 
-The step is captured once per buffer phase as a CUDA graph and replayed; K
-steps are timed with CUDA events between a barrier + synchronize on both
-sides, repeated in rounds of exactly K steps until about a second of GPU time
-has been covered (so the clock sampler sees the load); the median round is
-reported.  A second copy of each graph with CUDA events around the main
+The timed steps replay a CUDA graph of several consecutive steps (a multiple
+of the buffer phases that divides K, at most 16; one graph per step when there
+is none), so the kernels chain across steps inside a replay; K steps are timed
+with CUDA events between a barrier + synchronize on both sides, repeated in
+rounds of exactly K steps until about a second of GPU time has been covered
+(so the clock sampler sees the load); the median round is reported.  A second copy of each graph with CUDA events around the main
 kernel (the attention's split kernel, the fill kernel or the top-k scoring
 kernel) is replayed after every timed round; those events give the kernel's
 duration for the roofline line.
@@ -547,6 +548,10 @@ class TopkWorkload:
     kind = "topk"
     kernel = "topk_score_kernel"
     kernel_src = "clo_topk.cu"
+    # Steps chained inside one graph measured slower here (103.5 us a step with
+    # one graph a step, 109-114 us with 2-16 steps a graph), so each step is
+    # its own graph.
+    chain_steps = False
 
     def __init__(self, name, dev, rank: int, batch: int = 0):
         import torch
@@ -933,6 +938,28 @@ def run_ours(args):
         replay(i)
     torch.cuda.synchronize(dev)
 
+    # The timed steps replay a graph of `chunk` consecutive steps (a multiple
+    # of the buffer phases that divides K, at most 16), so the kernels chain
+    # through programmatic dependent launch from one step to the next inside
+    # a replay instead of stopping at a graph launch every step; K is still
+    # timed exactly.  Without such a multiple, or for a workload that measured
+    # slower chained (chain_steps = False), the per-step graphs are used.
+    K = args.steps
+    chunk = 1
+    for c in range(16 // W.phases * W.phases, W.phases - 1, -W.phases):
+        if c > 1 and K % c == 0 and getattr(W, "chain_steps", True):
+            chunk = c
+            break
+    multi = None
+    if chunk > 1:
+        multi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(multi):
+            for i in range(chunk):
+                W.launch(i)
+        torch.cuda.synchronize(dev)
+        multi.replay()  # one untimed replay of the chunk graph itself
+        torch.cuda.synchronize(dev)
+
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -940,7 +967,6 @@ def run_ours(args):
         gpu_id = str(local)
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
-    K = args.steps
     rounds, attn_ms = [], []
     t_start = time.perf_counter()
     step = args.warmup
@@ -950,9 +976,14 @@ def run_ours(args):
         barrier(pg)
         torch.cuda.synchronize(dev)
         ev0.record(stream)
-        for _ in range(K):
-            replay(step)
-            step += 1
+        if multi is not None:
+            for _ in range(K // chunk):
+                multi.replay()
+            step += K
+        else:
+            for _ in range(K):
+                replay(step)
+                step += 1
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(pg)
@@ -1045,7 +1076,7 @@ def run_ours(args):
         "gpu_launches": W.launches_per_step() * K,
         "timing": {"rounds": len(rounds), "round_ms_median": ms_round,
                    "round_ms_min": min(rounds), "round_ms_max": max(rounds),
-                   "graph_phases": W.phases},
+                   "graph_phases": W.phases, "graph_steps": chunk},
         "clocks": clocks,
     }
     line["peaks"] = {"measured_hbm_gbs": peak_hbm()[0], "nominal_hbm_gbs": NOMINAL_HBM_GBS,
