@@ -109,6 +109,21 @@ def test_ranges_cross_segments_in_both_parts(num_ctas):
     check_small(small_case(13, 8, 32, 8, 2048, 330, 2), num_ctas, "weighted cut")
 
 
+def test_index_order_does_not_matter():
+    """The Cache Buffer indices of each head in random, ascending and reversed
+    order name the same token set: the outputs agree within the bound of the
+    split-count test.  Only the order of the tiles differs, and with it the
+    running maximum at each tile, which sets how each softmax weight rounds
+    to fp16 for the P.V product (2^-11 relative a weight)."""
+    q, cbK, cbV, idx, pK, pV, pid = small_case(14, 3, 32, 8, 2500, 700, 2)
+    outs = []
+    for order in (idx, np.sort(idx, axis=-1), np.sort(idx, axis=-1)[..., ::-1]):
+        outs.append(run_gpu(*to_dev(q, cbK, cbV, np.ascontiguousarray(order), pK, pV, pid))[0])
+    for o in outs[1:]:
+        assert rel_l2(o, outs[0]) < 1e-3
+        assert np.max(np.abs(o - outs[0])) < 2e-3
+
+
 def test_tiny_config_from_generator():
     cfg = wl.CONFIGS["tiny"]
     q, _ = wl.queries_and_labels(cfg, 0, "cpu")
