@@ -229,7 +229,7 @@ def test_header_is_plain_c_and_links(L, tmp_path):
         "    /* the host-only planner, called from C: one layer of 4 heads */\n"
         "    float tau[4] = {0.8f, -0.5f, 0.6f, 0.0f}, sh[4] = {0.1f, 0.9f, 0.3f, 0.95f};\n"
         "    double D[4]; int32_t np_, npers[1], ids[4];\n"
-        "    if (clo_plan_persistent(tau, sh, 1, 4, 0.1f, 1e-4, 1e10, 5e5, D, &np_, npers, ids)\n"
+        "    if (clo_plan_persistent(tau, sh, 1, 4, 0.1f, 1e-4, 5e9, 5e5, D, &np_, npers, ids)\n"
         "        != CLO_OK) return 6;\n"
         '    printf("%d %d %d %d %d\\n", np_, npers[0], ids[0], ids[1], ids[2]);\n'
         "    return 0;\n}\n")
@@ -243,6 +243,6 @@ def test_header_is_plain_c_and_links(L, tmp_path):
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     # the same plan through the Python binding
     ref = clo.clo_plan_persistent([[0.8, -0.5, 0.6, 0.0]], [[0.1, 0.9, 0.3, 0.95]], 0.1, 1e-4,
-                                  1e10, 5e5)
+                                  5e9, 5e5)
     want = [ref["n_p"], int(ref["n_persist"][0])] + [int(x) for x in ref["persist_ids"][0][:3]]
     assert [int(x) for x in r.stdout.split()] == want, (r.stdout, want)
