@@ -54,7 +54,7 @@ if ROOT not in sys.path:
 import workloads as wl  # noqa: E402
 
 METRIC = ("µs per layer-step and achieved HBM GB/s (% of GB300 peak) for lookup+attention")
-DEFAULT_WORKLOAD = "llama3_8b_layer_b8_32k"
+DEFAULT_WORKLOAD = "qwen25_14b_step_b16_64k"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 L2_BYTES = 129 * 2 ** 20
@@ -149,20 +149,38 @@ class HybridWorkload:
         self.q_all = torch.empty((self.n_inst, cfg.B, cfg.Hq, cfg.d), dtype=torch.float16,
                                  device=dev)
         self.io_all = torch.zeros((self.n_inst, row), dtype=torch.uint8, device=dev)
+        # With label_reset, every set's labels sit in one buffer and each step
+        # starts by copying the drawn labels back over it, so the same groups
+        # miss every step (a miss replaces the group's labels with q).
+        self.lab_all = torch.empty((self.n_inst, cfg.B, cfg.Hq, cfg.d), dtype=torch.float16,
+                                   device=dev)
+        if cfg.miss_fill and schedule == "stream":
+            raise SystemExit("the miss-path fill runs with the fused or serial schedule")
         for i in range(self.n_inst):
             li = i + 1000 * rank
             res = self.io_all[i, out_bytes:out_bytes + res_bytes]
-            q0, lab = wl.queries_and_labels(cfg, li, dev)
+            q0, lab0 = wl.queries_and_labels(cfg, li, dev)
             q = self.q_all[i]
             q.copy_(q0)
-            del q0
+            lab = self.lab_all[i]
+            lab.copy_(lab0)
+            del q0, lab0
             has_cb = cfg.Np < cfg.Hkv
             cbK, cbV, idx = wl.cache_buffer(cfg, li, dev) if has_cb else (None, None, None)
             pK, pV = wl.persistent_cache(cfg, li, dev) if cfg.Np > 0 else (None, None)
+            srcK = srcV = None
+            if cfg.miss_fill:
+                # The full KV copy the missed heads' rows come from; the fill
+                # writes each missed head's rows idx[b][g] (the token itself,
+                # token-addressed), which the next attention then reads.
+                srcK, srcV = wl.full_kv(cfg, li, dev)
+                if cfg.miss_fill == "host":
+                    srcK, srcV = srcK.cpu().pin_memory(), srcV.cpu().pin_memory()
             s_np = wl.importance(cfg, li)
             s_all.append(s_np)
             self.inst.append(dict(
                 q=q, labels=lab, labels0=lab.clone(), cbK=cbK, cbV=cbV, idx=idx, pK=pK, pV=pV,
+                srcK=srcK, srcV=srcV,
                 pid=torch.from_numpy(wl.persist_ids(cfg, li)).to(dev),
                 pmask=torch.from_numpy(wl.persist_mask(cfg, li)).to(dev),
                 w=torch.from_numpy(s_np).to(dev),
@@ -182,21 +200,59 @@ class HybridWorkload:
                    max(1, n_tiles // 8))
         self.attn_kernels = 2 if ctas >= 2 else 1
         self.phases = self.n_inst // math.gcd(self.L, self.n_inst)
+        self.lab0_all = self.lab_all.clone()
+        self.restore = clo.prepare_copies([(self.lab_all, self.lab0_all)]) \
+            if cfg.label_reset else None
+        self.misses_per_step = self._count_misses()
+
+    def _count_misses(self) -> float:
+        """Misses of one step's L lookups, averaged over the buffer sets (one
+        lookup per set on the drawn labels; with label_reset every step sees
+        those labels, otherwise later lookups of a set hit after its first)."""
+        torch, clo, cfg = self.torch, self.clo, self.cfg
+        clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+        n = 0
+        for j, it in enumerate(self.inst):
+            lab = it["labels0"].clone()
+            clo.clo_lookup_update(it["q"], lab, it["w"], self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv],
+                                  it["pmask"], it["flag"], it["sim"], it["miss"], it["nmiss"])
+            n += int(it["nmiss"].item())
+        torch.cuda.synchronize()
+        return n / self.n_inst * self.L if cfg.label_reset else 0.0
 
     def instance(self, step: int, layer: int):
         return self.inst[(step * self.L + layer) % self.n_inst]
 
+    def miss_bytes_per_step(self) -> int:
+        """Bytes the misses of a step move: each missed group's G new labels
+        and its miss-list entry; with the fill, its k K and V rows read from
+        the full KV copy and written into the Cache Buffer, and the k row ids."""
+        cfg = self.cfg
+        per = cfg.G * cfg.d * HALF + 4
+        if cfg.miss_fill:
+            per += cfg.k * (2 * cfg.d * HALF * 2 + 4)
+        return int(round(self.misses_per_step * per))
+
     def bytes_per_step(self) -> int:
         return self.L * (hybrid_attn_bytes(self.cfg) + hybrid_lookup_bytes(self.cfg)) + \
-            self.n_inst * (self.cfg.Hq + self.cfg.Hkv) * 4
+            self.n_inst * (self.cfg.Hq + self.cfg.Hkv) * 4 + self.miss_bytes_per_step()
 
     def attn_bytes_per_launch(self) -> int:
         return hybrid_attn_bytes(self.cfg)
 
     def launches_per_step(self) -> int:
+        extra = (1 if self.restore is not None else 0) + (self.L if self.cfg.miss_fill else 0)
         if self.schedule == "fused":  # main kernel + merge launch carrying the lookup
-            return 1 + self.L * 2
-        return 1 + self.L * (1 + self.attn_kernels)
+            return 1 + self.L * 2 + extra
+        return 1 + self.L * (1 + self.attn_kernels) + extra
+
+    def _fill(self, step: int, l: int):
+        """The miss path of layer l's lookup: its missed heads' rows from the
+        full KV copy into the Cache Buffer (read on the device from the
+        lookup's miss list)."""
+        it = self.instance(step, l)
+        self.clo.clo_fill_cache_buffer(it["srcK"], it["srcV"], it["idx"], None, it["cbK"],
+                                       it["cbV"], it["miss"], it["nmiss"], err_flag=self.err)
 
     def _lookup(self, step: int, l: int):
         cfg = self.cfg
@@ -236,15 +292,21 @@ class HybridWorkload:
         attention 0 of a step always follows its lookup).  With the "serial"
         schedule every layer runs lookup then attention on one stream."""
         clo, cfg, torch = self.clo, self.cfg, self.torch
+        if self.restore is not None:
+            self.restore()
         if self.schedule == "fused":
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
             for l in range(self.L):
                 self._attention_lookup(step, l, None if attn_events is None else attn_events[l])
+                if cfg.miss_fill:
+                    self._fill(step, l + 1)
             return
         if self.schedule == "serial":
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
             for l in range(self.L):
                 self._lookup(step, l)
+                if cfg.miss_fill:
+                    self._fill(step, l)
                 self._attention(step, l, None if attn_events is None else attn_events[l])
             return
         main = torch.cuda.current_stream()
@@ -287,6 +349,11 @@ class HybridWorkload:
         self.e2e_tau = clo.prepare_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
         self.e2e_layer = []
         for j, it in enumerate(self.inst):
+            def fill_of(x):
+                return (clo.prepare_fill_cache_buffer(x["srcK"], x["srcV"], x["idx"], None,
+                                                      x["cbK"], x["cbV"], x["miss"], x["nmiss"],
+                                                      err_flag=self.err),) \
+                    if cfg.miss_fill else ()
             if self.schedule == "fused":
                 # This layer's attention with the next layer's lookup.
                 jn = (j + 1) % self.n_inst
@@ -295,19 +362,22 @@ class HybridWorkload:
                 calls = (clo.prepare_hybrid_decode_attn_lookup(
                     it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"], it["pV"], it["pid"],
                     it["out"], self.ws, nx["q"], nx["labels"], nx["w"], tau, nx["pmask"],
-                    nx["flag"], nx["sim"], nx["miss"], nx["nmiss"], err_flag=self.err),)
+                    nx["flag"], nx["sim"], nx["miss"], nx["nmiss"], err_flag=self.err),) + \
+                    fill_of(nx)
             else:
                 tau = self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv]
                 calls = (clo.prepare_lookup_update(it["q"], it["labels"], it["w"], tau,
                                                    it["pmask"], it["flag"], it["sim"], it["miss"],
-                                                   it["nmiss"]),
-                         clo.prepare_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"],
-                                                        it["pK"], it["pV"], it["pid"], it["out"],
-                                                        self.ws, err_flag=self.err))
+                                                   it["nmiss"]),) + fill_of(it) + \
+                    (clo.prepare_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"],
+                                                    it["pK"], it["pV"], it["pid"], it["out"],
+                                                    self.ws, err_flag=self.err),)
             self.e2e_layer.append(calls)
 
     def e2e_step(self, step: int):
         self.e2e_pipe.step_in()
+        if self.restore is not None:
+            self.restore()
         self.e2e_tau()
         for l in range(self.L):
             for call in self.e2e_layer[(step * self.L + l) % self.n_inst]:
@@ -372,7 +442,21 @@ class HybridWorkload:
                     "serial": "before each layer's attention, same stream"}[self.schedule],
                 "physical_buffer_sets": self.n_inst,
                 "l2": f"inputs larger than L2: a buffer is re-read after "
-                      f"{self.reuse_distance() / 2**30:.2f} GiB of other reads"}
+                      f"{self.reuse_distance() / 2**30:.2f} GiB of other reads"} | (
+            {"importance": "s = 1 on every head (tau = eta)",
+             "query_label_cosine": f"U({c.c_lo}, {c.c_hi})",
+             "label_reset": "each step first copies the drawn labels back (one libclo copy "
+                            "launch, in the timed step; its bytes are not counted), so the "
+                            "same groups miss every step",
+             "misses_per_step": self.misses_per_step,
+             "miss_bytes_per_step": self.miss_bytes_per_step(),
+             "miss_fill": ({"host": "after each lookup, the missed heads' k rows from the full "
+                                    "KV copy in pinned host memory (read over NVLink-C2C) into "
+                                    "the Cache Buffer rows the next attention reads",
+                            "device": "after each lookup, the missed heads' k rows from a full "
+                                      "KV copy in HBM into the Cache Buffer"}
+                           .get(c.miss_fill, "none"))}
+            if c.label_reset else {})
 
     def reuse_distance(self) -> int:
         per = hybrid_attn_bytes(self.cfg)
@@ -888,6 +972,8 @@ def run_ours(args):
         cfg = wl.CONFIGS[args.workload]
         if args.batch:
             cfg = dataclasses.replace(cfg, B=args.batch)
+        if args.ring and cfg.L > 1:
+            cfg = dataclasses.replace(cfg, ring=args.ring)
         W = HybridWorkload(cfg, dev, rank, args.replicas, schedule=args.lookup_schedule)
     elif args.workload in wl.FILL_CONFIGS:
         W = FillWorkload(args.workload, dev, rank, args.batch)
@@ -1070,7 +1156,14 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": kernel, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": W.attn_bytes_per_launch(),
-                     "launch_ms_mean": attn_ms_mean, "launch_samples": len(attn_ms)},
+                     "launch_ms_mean": attn_ms_mean, "launch_samples": len(attn_ms),
+                     "launch_ms_source": "CUDA events recorded around the kernel in a second copy "
+                                         "of the step graph, replayed after each timed round; "
+                                         "the event nodes serialise the launches next to the "
+                                         "kernel (no programmatic overlap), so the duration is "
+                                         "a little longer than the kernel's share of a chained "
+                                         "step",
+                     "layer_step_ms": ms_step / W.L},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": W.launches_per_step() * K,
@@ -1149,6 +1242,10 @@ def main(argv=None):
                          "then attention for every layer on one stream")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases)")
+    ap.add_argument("--ring", type=int, default=0,
+                    help="physical layer buffers of a multi-layer workload (0 = the workload's "
+                         "own: one per layer, or its ring); smaller device footprints for "
+                         "profiling")
     ap.add_argument("--replicas", type=int, default=0,
                     help="physical buffer sets of a one-layer workload (0 = auto, >1 GB apart)")
     args = ap.parse_args(argv)

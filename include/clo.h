@@ -132,6 +132,18 @@ clo_status clo_thresholds(const float* s, int n_kv, int group, float eta,
                           float n_exp, float* tau, cudaStream_t stream);
 
 /*
+ * clo_thresholds_host -- the same thresholds (CLO Eqs. 7-9), computed on the
+ * host for callers that set tau once per model or configuration and keep it:
+ * s and tau are HOST arrays ([n_kv * group] and [n_kv] fp32), the call is
+ * synchronous and touches no GPU.  fp32 arithmetic in the kernel's order (the
+ * group mean of s, then Eqs. 7-9 with the host C library's acosf, powf,
+ * cosf); it agrees with clo_thresholds and with the fp64 definition within
+ * 1e-6.  Same argument rules as clo_thresholds (n_kv == 0 is a no-op).
+ */
+clo_status clo_thresholds_host(const float* s, int n_kv, int group, float eta, float n_exp,
+                               float* tau);
+
+/*
  * clo_lookup_update -- fused head-wise approximate-cache lookup and query-label
  * update (CLO section 2 "head-wise approximate cache" and "fused cache lookup
  * + query label update kernel"; Eq. 10; section 3 Fig. 7).  One launch reads
@@ -334,8 +346,10 @@ clo_status clo_hybrid_decode_attn_lookup(
  *  - Returns CLO_ERR_WORKSPACE, launching nothing, when the problem needs more
  *    than that (clo_hybrid_workspace_size(B, Hq, Hkv, d, num_ctas) > 8 MiB).
  *  - The first call on each device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.  CLO_ERR_CUDA if the lookup fails.
+ *    that device current) and caches it for that device's context; make that
+ *    first call before any stream capture.  A call in a new context on the
+ *    device (after cudaDeviceReset) looks it up again, and is then again a
+ *    first call.  CLO_ERR_CUDA if the lookup fails.
  *  - It never calls cudaMalloc, cudaFree or any allocating routine.
  *  - All calls share the one array and it keeps the previous call's
  *    contents; nothing in it needs to start at zero.  Calls on one device

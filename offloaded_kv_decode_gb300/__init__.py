@@ -56,6 +56,7 @@ _SIGS = {
     "clo_check_error_flag": ([ctypes.c_int32], _I),
     "clo_copy_async": ([_P, _I, _P], _I),
     "clo_thresholds": ([_P, _I, _I, _F, _F, _P, _P], _I),
+    "clo_thresholds_host": ([_P, _I, _I, _F, _F, _P], _I),
     "clo_lookup_update": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "clo_fill_cache_buffer": ([_P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P,
                                _P], _I),
@@ -213,8 +214,8 @@ class CloCopy(ctypes.Structure):
 
 
 def _copies_call(pairs):
-    """pairs: (dst, src) tensors, one on the GPU and the other in pinned host memory,
-    contiguous, with the same number of bytes."""
+    """pairs: (dst, src) tensors, contiguous, with the same number of bytes; each
+    on the GPU or in pinned host memory, at least one of the two on the GPU."""
     pairs = list(pairs)
     arr = (CloCopy * max(len(pairs), 1))()
     for i, (dst, src) in enumerate(pairs):
@@ -228,8 +229,8 @@ def _copies_call(pairs):
             if not t.is_cuda and not t.is_pinned():
                 raise CloError(f"copy {i}: {name} must be a CUDA tensor or pinned host memory",
                                CLO_ERR_INVALID_ARG)
-        if dst.is_cuda == src.is_cuda:
-            raise CloError(f"copy {i}: one side must be host memory and the other CUDA memory",
+        if not dst.is_cuda and not src.is_cuda:
+            raise CloError(f"copy {i}: host-to-host copies are not made here",
                            CLO_ERR_INVALID_ARG)
         nb = dst.numel() * dst.element_size()
         if nb != src.numel() * src.element_size():
@@ -239,7 +240,7 @@ def _copies_call(pairs):
 
 
 def clo_copy_async(pairs: Sequence, stream=None):
-    """Issues the copies (dst, src) in order on the stream (pinned host <-> CUDA)."""
+    """Issues the copies (dst, src) on the stream (pinned host <-> CUDA, or CUDA <-> CUDA)."""
     _run(_copies_call(pairs), stream)
 
 
@@ -262,6 +263,22 @@ def prepare_thresholds(s, tau, group: int = 1, eta: float = 0.8, n_exp: float = 
                        stream=None) -> PreparedCall:
     """clo_thresholds on fixed buffers, checked once (see PreparedCall)."""
     return PreparedCall(*_thresholds_call(s, tau, group, eta, n_exp), stream)
+
+
+def clo_thresholds_host(s, n_kv: int, group: int = 1, eta: float = 0.8, n_exp: float = 3.0):
+    """The same thresholds computed by the library on the host (no GPU):
+    s is an array-like of n_kv*group fp32 scores; returns tau as a float32
+    numpy array [n_kv]."""
+    import numpy as np
+
+    sv = np.ascontiguousarray(np.asarray(s, dtype=np.float32).ravel())
+    if sv.size != n_kv * group:
+        raise CloError("s must hold n_kv*group scores", CLO_ERR_INVALID_ARG)
+    tau = np.zeros(max(int(n_kv), 1), dtype=np.float32)
+    _check(lib().clo_thresholds_host(sv.ctypes.data if sv.size else None, int(n_kv), int(group),
+                                     float(eta), float(n_exp), tau.ctypes.data),
+           "clo_thresholds_host")
+    return tau[:n_kv].copy()
 
 
 def _thresholds_call(s, tau, group, eta, n_exp):

@@ -1430,19 +1430,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device with that device current, then cached.
+// with the device current, once per device and context, then cached; a new
+// context on the device (after cudaDeviceReset) is looked up again.
 static void* noalloc_scratch_address() {
     static std::mutex mu;
     static void* addr[64] = {nullptr};
+    static unsigned long long ctx_of[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    if (ctx != 0 && addr[dev] != nullptr && ctx_of[dev] == ctx) return addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+    ctx_of[dev] = current_context_id();  // the lookup made the primary context current
+    return p;
 }
 }  // namespace clo
 

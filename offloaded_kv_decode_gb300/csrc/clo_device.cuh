@@ -1,6 +1,7 @@
 // clo_device.cuh -- small inline-PTX building blocks for the sm_103a kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -182,20 +183,56 @@ inline int device_sm_count() {
     return cache[dev];
 }
 
+// Identifier of the calling thread's current CUDA context, unique for the
+// life of the process; 0 when no context is current or the driver cannot
+// say.  Per-device caches of context state (kernel attributes, symbol
+// addresses) are keyed on it, so they are rebuilt after cudaDeviceReset
+// replaces a device's primary context.
+inline unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(f);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 // Applies the launch attributes every libclo kernel shares, once per
-// (kernel, device): the maximum shared-memory carveout (so consecutive libclo
-// kernels never make the SMs switch their L1/shared split) and, if
-// dyn_smem > 48 KB, the opt-in dynamic shared-memory size.
+// (kernel, context): the maximum shared-memory carveout (so consecutive
+// libclo kernels never make the SMs switch their L1/shared split) and, if
+// dyn_smem > 48 KB, the opt-in dynamic shared-memory size.  The attributes
+// belong to the context, so a new context (after cudaDeviceReset) gets them
+// again; with no context id they are set on every call.
 inline bool prepare_kernel(const void* func, int dyn_smem) {
     static std::mutex mu;
     static const void* done_func[64];
-    static int done_dev[64];
+    static unsigned long long done_ctx[64];
+    static int done_smem[64];
     static int n_done = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n_done; ++i)
-        if (done_func[i] == func && done_dev[i] == dev) return true;
+    if (ctx != 0)
+        for (int i = 0; i < n_done; ++i)
+            if (done_func[i] == func && done_ctx[i] == ctx && done_smem[i] >= dyn_smem) return true;
     if (cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return false;
@@ -203,11 +240,15 @@ inline bool prepare_kernel(const void* func, int dyn_smem) {
         cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem) !=
             cudaSuccess)
         return false;
-    if (n_done < 64) {
-        done_func[n_done] = func;
-        done_dev[n_done] = dev;
-        ++n_done;
-    }
+    if (ctx == 0) return true;
+    int slot = -1;
+    for (int i = 0; i < n_done && slot < 0; ++i)
+        if (done_func[i] == func && done_ctx[i] == ctx) slot = i;
+    if (slot < 0 && n_done < 64) slot = n_done++;
+    if (slot < 0) slot = static_cast<int>(reinterpret_cast<uintptr_t>(func) % 64);  // full: reuse
+    done_func[slot] = func;
+    done_ctx[slot] = ctx;
+    done_smem[slot] = dyn_smem;
     return true;
 }
 

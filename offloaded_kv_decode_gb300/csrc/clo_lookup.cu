@@ -67,6 +67,26 @@ extern "C" clo_status clo_thresholds(const float* s, int n_kv, int group, float 
                : CLO_ERR_CUDA;
 }
 
+// The same map on the host in fp32, in the kernel's order: the group mean of
+// s, then Eqs. 7-9 with the host C library's acosf, powf and cosf.
+extern "C" clo_status clo_thresholds_host(const float* s, int n_kv, int group, float eta,
+                                          float n_exp, float* tau) {
+    if (n_kv < 0 || group < 1) return CLO_ERR_INVALID_ARG;
+    if (!(eta >= -1.f && eta <= 1.f) || !(n_exp >= 0.f)) return CLO_ERR_INVALID_ARG;
+    if (n_kv == 0) return CLO_OK;
+    if (s == nullptr || tau == nullptr) return CLO_ERR_INVALID_ARG;
+    const float theta_star = acosf(eta);                              // Eq. 7
+    for (int g = 0; g < n_kv; ++g) {
+        float acc = 0.f;
+        for (int j = 0; j < group; ++j) acc += s[static_cast<size_t>(g) * group + j];
+        const float sg = acc / static_cast<float>(group);
+        const float lam = powf(sg, n_exp);                            // Eq. 8
+        const float theta = lam * theta_star + (1.f - lam) * PI_F;    // Eq. 9
+        tau[g] = cosf(theta);
+    }
+    return CLO_OK;
+}
+
 extern "C" clo_status clo_lookup_update(const clo_half* q, clo_half* labels, const float* w_q,
                                         const float* tau_kv, const uint8_t* persist_mask, int B,
                                         int Hq, int Hkv, int d, uint8_t* flag, float* sim,

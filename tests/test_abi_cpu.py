@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 17, names
+    assert len(names) == 18, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -231,6 +231,10 @@ def test_header_is_plain_c_and_links(L, tmp_path):
         "    double D[4]; int32_t np_, npers[1], ids[4];\n"
         "    if (clo_plan_persistent(tau, sh, 1, 4, 0.1f, 1e-4, 5e9, 5e5, D, &np_, npers, ids)\n"
         "        != CLO_OK) return 6;\n"
+        "    /* host thresholds, Eqs. 7-9: s = 1 gives eta, s = 0 gives -1 */\n"
+        "    float s3[3] = {1.0f, 0.0f, 0.5f}, t3[3];\n"
+        "    if (clo_thresholds_host(s3, 3, 1, 0.8f, 3.0f, t3) != CLO_OK) return 7;\n"
+        "    if (t3[0] < 0.799999f || t3[0] > 0.800001f || t3[1] > -0.999999f) return 8;\n"
         '    printf("%d %d %d %d %d\\n", np_, npers[0], ids[0], ids[1], ids[2]);\n'
         "    return 0;\n}\n")
     exe = tmp_path / "use_clo"

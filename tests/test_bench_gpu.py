@@ -19,6 +19,10 @@ pytestmark = pytest.mark.gpu
     ["--workload", "fill_hbm_llama3_8b_b8_32k", "--batch", "1"],
     ["--workload", "fill_c2c_llama3_8b_b8_32k", "--batch", "1"],
     ["--workload", "topk_llama3_8b_b8_32k", "--batch", "1"],
+    ["--workload", "qwen25_14b_step_b16_64k", "--batch", "1"],
+    ["--workload", "llama3_8b_layer_b8_32k_miss", "--batch", "2"],
+    ["--workload", "llama3_8b_layer_b8_32k_miss", "--batch", "2", "--lookup-schedule", "serial"],
+    ["--workload", "llama3_8b_layer_b8_32k_miss_fill", "--batch", "1"],
 ], ids=lambda a: "_".join(x.lstrip("-") for x in a[1::2] if x not in ("--batch",)))
 def test_bench_line(args):
     buf = io.StringIO()
@@ -36,3 +40,7 @@ def test_bench_line(args):
     assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
     if "lookup" in d:
         assert d["lookup"]["looked_up_heads"] > 0 and d["tokens_per_s"] > 0
+    if "_miss" in d["config"]["workload"]:
+        # the misses recur every step (labels restored) and their bytes are counted
+        assert d["config"]["misses_per_step"] > 0 and d["config"]["miss_bytes_per_step"] > 0
+        assert 0.0 < d["lookup"]["hit_rate"] < 1.0

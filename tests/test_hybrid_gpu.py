@@ -3,8 +3,8 @@
 Small cases run the whole oracle (several tiles per head, ragged tails,
 GQA 1/4/5/8, no / some / all persistent heads, token-addressed and compact
 Cache Buffers, several CTA counts).  The full-size workloads run the kernel in
-the configuration the benchmark uses and check sampled (batch, KV head) groups
-one by one against the oracle's dense attention over rows gathered on the host.
+the configuration the benchmark uses and check every (batch, KV head) group
+against the oracle's dense attention over the group's rows.
 """
 import numpy as np
 import pytest
@@ -13,7 +13,7 @@ import torch
 import oracle
 import offloaded_kv_decode_gb300 as clo
 import workloads as wl
-from gpu_util import LSE_ATOL, assert_close, dev, rel_l2, scale_for
+from gpu_util import LSE_ATOL, assert_close, dev, parallel_map, rel_l2, scale_for
 
 pytestmark = pytest.mark.gpu
 
@@ -158,13 +158,18 @@ def test_bad_persist_ids_zero_everything():
         assert np.all(got == 0) and np.all(np.isneginf(lse))
 
 
-# ---------------------------------------------------------------- full size, sampled
+# ---------------------------------------------------------------- full size, every group
 
-def full_size_check(name, samples, num_layers=1):
+def full_size_check(name, layers=(0,), groups=None):
+    """The workload at full size, in the launch configuration the benchmark
+    uses; every (batch row, KV head) group (or the `groups` subset) of each
+    layer compared with the oracle's dense attention over the group's rows,
+    gathered on the GPU and copied to the host.  Returns the groups checked."""
     cfg = wl.CONFIGS[name]
     scale = scale_for()
     orc = oracle.get()
-    for layer in range(num_layers):
+    checked = 0
+    for layer in layers:
         q, _ = wl.queries_and_labels(cfg, layer, dev())
         cbK, cbV, idx = wl.cache_buffer(cfg, layer, dev())
         pK, pV = wl.persistent_cache(cfg, layer, dev())
@@ -174,30 +179,33 @@ def full_size_check(name, samples, num_layers=1):
         assert err == 0
         qh = q.cpu().numpy()
         G = cfg.G
-        for (b, g) in samples(cfg, pid_np):
+        todo = groups(cfg, pid_np) if groups is not None else \
+            [(b, g) for b in range(cfg.B) for g in range(cfg.Hkv)]
+        rows = {}
+        for (b, g) in todo:
             if g in pid_np.tolist():
                 j = pid_np.tolist().index(g)
-                K, V = pK[b, j].cpu().numpy(), pV[b, j].cpu().numpy()
+                rows[(b, g)] = (pK[b, j].cpu().numpy(), pV[b, j].cpu().numpy())
             else:
-                rows = idx[b, g].cpu().numpy()
-                K = cbK[b, g].cpu().numpy()[rows]
-                V = cbV[b, g].cpu().numpy()[rows]
-            ref, ref_lse = orc.attention_dense(qh[b, g * G:(g + 1) * G], K, V, scale)
-            assert_close(got[b, g * G:(g + 1) * G], ref, f"{name} b{b} g{g}")
+                sel = idx[b, g].long()
+                rows[(b, g)] = (cbK[b, g][sel].cpu().numpy(), cbV[b, g][sel].cpu().numpy())
+        refs = parallel_map(
+            lambda bg: orc.attention_dense(qh[bg[0], bg[1] * G:(bg[1] + 1) * G], *rows[bg], scale),
+            todo)
+        for (b, g), (ref, ref_lse) in zip(todo, refs):
+            assert_close(got[b, g * G:(g + 1) * G], ref, f"{name} layer {layer} b{b} g{g}")
             assert np.max(np.abs(lse[b, g * G:(g + 1) * G] - ref_lse)) < LSE_ATOL
-        del q, cbK, cbV, idx, pK, pV
+        checked += len(todo)
+        del q, cbK, cbV, idx, pK, pV, rows
         torch.cuda.empty_cache()
+    print(f"{name}: {checked} groups checked against the oracle over layers {list(layers)}")
+    return checked
 
 
-def _samples(cfg, pid):
-    rng = np.random.Generator(np.random.PCG64(cfg.seed))
-    cached = [g for g in range(cfg.Hkv) if g not in pid.tolist()]
-    out = [(0, int(pid[0])), (cfg.B - 1, int(cached[-1])), (0, int(cached[0]))]
-    out.append((int(rng.integers(cfg.B)), int(rng.choice(cached))))
-    return out
-
-
-@pytest.mark.parametrize("name", ["llama3_8b_layer_b8_32k", "llama3_8b_step_b1_128k",
-                                  "llama3_8b_step_b4_128k", "qwen25_14b_step_b16_64k"])
-def test_full_size_sampled(name):
-    full_size_check(name, _samples)
+@pytest.mark.parametrize("name,layers", [("llama3_8b_layer_b8_32k", (0, 1)),
+                                         ("llama3_8b_step_b1_128k", (0, 1)),
+                                         ("llama3_8b_step_b4_128k", (0,)),
+                                         ("qwen25_14b_step_b16_64k", (0,))])
+def test_full_size_every_group(name, layers):
+    cfg = wl.CONFIGS[name]
+    assert full_size_check(name, layers) == len(layers) * cfg.B * cfg.Hkv

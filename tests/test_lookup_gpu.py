@@ -8,7 +8,7 @@ import torch
 import oracle
 import offloaded_kv_decode_gb300 as clo
 import workloads as wl
-from gpu_util import NEAR_TAU, dev
+from gpu_util import NEAR_TAU, assert_lookup_matches, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -34,34 +34,22 @@ def compare(q, lab, w, tau32, pm):
     """Runs both sides; returns the number of near-tau groups."""
     ref = oracle.get().lookup_update(q, lab, w.astype(np.float64), tau32.astype(np.float64), pm)
     got = run_gpu(q, lab, w, tau32, pm)
-    B, Hkv = ref["flag"].shape
-    G = q.shape[1] // Hkv
-    near = np.abs(ref["sim"] - tau32.astype(np.float64)[None, :]) < NEAR_TAU
-    if pm is not None:
-        near &= pm[None, :] == 0
-    ok = ~near
-    assert np.array_equal(got["flag"][ok], ref["flag"][ok]), "hit/miss flags differ"
-    assert np.max(np.abs(got["sim"].astype(np.float64) - ref["sim"])) < 1e-5
-    labg = got["labels"].view(np.uint16).reshape(B, Hkv, G, -1)
-    labr = ref["labels"].reshape(B, Hkv, G, -1)
-    assert np.array_equal(labg[ok], labr[ok]), "label updates differ"
-    near_ids = set(np.flatnonzero(near.ravel()).tolist())
-    gl = [x for x in got["miss_list"].tolist() if x not in near_ids]
-    rl = [x for x in ref["miss_list"].tolist() if x not in near_ids]
-    assert gl == rl, "miss list differs"
-    assert got["miss_list"].tolist() == sorted(got["miss_list"].tolist())
-    assert got["miss_count"] == int((got["flag"] == 1).sum())
-    return int(near.sum())
+    return assert_lookup_matches(ref, got, tau32, pm, q.shape[1] // tau32.size)
 
 
 def cfg_inputs(cfg, layer=0):
+    """The workload's lookup inputs; tau is the library's (clo_thresholds_host),
+    which both sides then take, and it must match the oracle's Eqs. 7-9."""
     q, lab = wl.queries_and_labels(cfg, layer, "cpu")
     s = wl.importance(cfg, layer)
-    tau = oracle.get().thresholds(s.astype(np.float64), cfg.Hkv, cfg.G, wl.ETA, wl.N_EXP)
-    return q.numpy(), lab.numpy(), s, tau.astype(np.float32), wl.persist_mask(cfg, layer)
+    tau = clo.clo_thresholds_host(s, cfg.Hkv, cfg.G, wl.ETA, wl.N_EXP)
+    ref = oracle.get().thresholds(s.astype(np.float64), cfg.Hkv, cfg.G, wl.ETA, wl.N_EXP)
+    assert np.max(np.abs(tau.astype(np.float64) - ref)) < 1e-6
+    return q.numpy(), lab.numpy(), s, tau, wl.persist_mask(cfg, layer)
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama3_8b_layer_b8_32k", "llama3_8b_step_b4_128k",
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b_layer_b8_32k", "llama3_8b_layer_b8_32k_miss",
+                                  "llama3_8b_step_b4_128k",
                                   "qwen25_14b_step_b16_64k"])
 def test_lookup_configs(name):
     cfg = wl.CONFIGS[name]

@@ -6,7 +6,7 @@ import torch
 import oracle
 import offloaded_kv_decode_gb300 as clo
 import workloads as wl
-from gpu_util import LSE_ATOL, assert_close, dev, scale_for
+from gpu_util import LSE_ATOL, assert_close, dev, parallel_map, scale_for
 
 pytestmark = pytest.mark.gpu
 
@@ -76,20 +76,32 @@ def test_bad_block_and_length_flagged():
     assert_close(got[[0, 3]], ref[[0, 3]], "untouched requests")
 
 
-def test_full_size_sampled():
+def test_full_size_many_pairs():
+    """The B256 workload at full size: every head of twelve requests (the
+    shortest, the longest, the first and last, and eight drawn at random),
+    384 (request, head) pairs against the oracle."""
     pc = wl.PAGED_CONFIGS["paged_llama2_7b_b256"]
     q, kc, vc, bt, cl = wl.paged_inputs(pc, dev())
     got, lse, err = run_gpu(q, kc, vc, bt, cl)
     assert err == 0
     orc = oracle.get()
     cln, btn, qn = cl.cpu().numpy(), bt.cpu().numpy(), q.cpu().numpy()
-    rs = [int(np.argmin(cln)), int(np.argmax(cln)), 0, pc.B - 1, 97]
+    rng = np.random.Generator(np.random.PCG64(pc.seed))
+    rs = [int(np.argmin(cln)), int(np.argmax(cln)), 0, pc.B - 1]
+    rs += [int(x) for x in rng.choice([r for r in range(pc.B) if r not in rs], 8, replace=False)]
+    pairs = [(r, h) for r in rs for h in range(pc.Hkv)]
+    rows = {}
     for r in rs:
         nb = -(-int(cln[r]) // 16)
         blocks = torch.from_numpy(btn[r, :nb].astype(np.int64)).to(dev())
-        for h in (0, 13, pc.Hkv - 1):
-            K = kc[blocks, h].reshape(-1, 128)[: cln[r]].cpu().numpy()
-            V = vc[blocks, h].reshape(-1, 128)[: cln[r]].cpu().numpy()
-            ref, ref_lse = orc.attention_dense(qn[r, h:h + 1], K, V, scale_for())
-            assert_close(got[r, h:h + 1], ref, f"paged r{r} h{h}")
-            assert abs(lse[r, h] - ref_lse[0]) < LSE_ATOL
+        Kr = kc[blocks].permute(1, 0, 2, 3).reshape(pc.Hkv, -1, 128)[:, : cln[r]].cpu().numpy()
+        Vr = vc[blocks].permute(1, 0, 2, 3).reshape(pc.Hkv, -1, 128)[:, : cln[r]].cpu().numpy()
+        rows[r] = (Kr, Vr)
+    G = pc.G
+    refs = parallel_map(lambda rh: orc.attention_dense(
+        qn[rh[0], rh[1] * G:(rh[1] + 1) * G], np.ascontiguousarray(rows[rh[0]][0][rh[1]]),
+        np.ascontiguousarray(rows[rh[0]][1][rh[1]]), scale_for()), pairs)
+    for (r, h), (ref, ref_lse) in zip(pairs, refs):
+        assert_close(got[r, h * G:(h + 1) * G], ref, f"paged r{r} h{h}")
+        assert np.max(np.abs(lse[r, h * G:(h + 1) * G] - ref_lse)) < LSE_ATOL
+    print(f"paged B256: {len(pairs)} (request, head) pairs checked against the oracle")

@@ -84,12 +84,18 @@ def test_copy_lists_may_not_overlap():
     assert torch.equal(d[:64].cpu(), h) and torch.equal(d[64:].cpu(), h)
 
 
-def test_copy_pairs_must_cross_the_link():
-    d = torch.empty(4, device=dev())
+def test_copy_pairs_device_or_pinned():
+    """Device-to-device copies are made too (a caller restoring state between
+    steps); host-to-host and mismatched sizes are refused."""
+    src = torch.arange(1000, dtype=torch.int32, device=dev())
+    d = torch.zeros(1000, dtype=torch.int32, device=dev())
+    clo.clo_copy_async([(d, src)])
+    torch.cuda.synchronize()
+    assert torch.equal(d, src)
     with pytest.raises(clo.CloError):
-        clo.prepare_copies([(d, torch.empty(4, device=dev()))])
+        clo.prepare_copies([(torch.empty(4).pin_memory(), torch.empty(4).pin_memory())])
     with pytest.raises(clo.CloError):
-        clo.prepare_copies([(d, torch.empty(5).pin_memory())])
+        clo.prepare_copies([(torch.empty(4, device=dev()), torch.empty(5).pin_memory())])
 
 
 def _layer(cfg, layer):

@@ -25,3 +25,6 @@ def test_thresholds_vs_oracle(group, eta, n):
     got = tau.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(got - ref)) < 1e-6
     assert abs(got[0] - eta) < 1e-6 and abs(got[1] + 1.0) < 1e-6
+    # and the library's host variant of the same map
+    host = clo.clo_thresholds_host(s, n_kv, group, eta, n).astype(np.float64)
+    assert np.max(np.abs(got - host)) < 1e-6
