@@ -120,7 +120,8 @@ class HybridWorkload:
     kind = "hybrid"
     e2e_path = PIPELINED_E2E
 
-    def __init__(self, cfg, dev, rank: int, replicas: int = 0, schedule: str = "fused"):
+    def __init__(self, cfg, dev, rank: int, replicas: int = 0, schedule: str = "fused",
+                 side_ctas=None):
         import torch
         import offloaded_kv_decode_gb300 as clo
 
@@ -154,8 +155,6 @@ class HybridWorkload:
         # miss every step (a miss replaces the group's labels with q).
         self.lab_all = torch.empty((self.n_inst, cfg.B, cfg.Hq, cfg.d), dtype=torch.float16,
                                    device=dev)
-        if cfg.miss_fill and schedule == "stream":
-            raise SystemExit("the miss-path fill runs with the fused or serial schedule")
         for i in range(self.n_inst):
             li = i + 1000 * rank
             res = self.io_all[i, out_bytes:out_bytes + res_bytes]
@@ -200,10 +199,25 @@ class HybridWorkload:
                    max(1, n_tiles // 8))
         self.attn_kernels = 2 if ctas >= 2 else 1
         self.phases = self.n_inst // math.gcd(self.L, self.n_inst)
+        # "overlap": the next layer's fill runs on a second stream beside this
+        # layer's attention.  The fill takes side_ctas CTAs (each fits in the
+        # room of one attention CTA) and the attention grid leaves that many of
+        # its 3 x SMs slots free, so both are resident at once.  (None: 96 with
+        # that schedule, else the full grids; a number applies to any schedule.)
+        if side_ctas is None:
+            side_ctas = 96 if schedule == "overlap" else 0
+        self.side_ctas = side_ctas
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.main_ctas = max(1, 3 * sms - self.side_ctas) if self.side_ctas else 0
+        self.fill_ctas = self.side_ctas
         self.lab0_all = self.lab_all.clone()
         self.restore = clo.prepare_copies([(self.lab_all, self.lab0_all)]) \
             if cfg.label_reset else None
         self.misses_per_step = self._count_misses()
+        if cfg.miss_fill:
+            # The fill moves the step's rows over the host link (or reads and
+            # writes them in HBM): the roofline line covers it.
+            self.kernel, self.kernel_src = "fill_kernel", "clo_fill.cu"
 
     def _count_misses(self) -> float:
         """Misses of one step's L lookups, averaged over the buffer sets (one
@@ -238,7 +252,25 @@ class HybridWorkload:
             self.n_inst * (self.cfg.Hq + self.cfg.Hkv) * 4 + self.miss_bytes_per_step()
 
     def attn_bytes_per_launch(self) -> int:
-        return hybrid_attn_bytes(self.cfg)
+        """Bytes the roofline kernel moves per launch: the attention's
+        algorithmic bytes, or with the miss-path fill the fill's rows (read
+        over the host link; read and written, plus the row ids, from HBM),
+        at the mean misses of a launch."""
+        cfg = self.cfg
+        if not cfg.miss_fill:
+            return hybrid_attn_bytes(cfg)
+        rows = self.misses_per_step / self.L * cfg.k
+        if cfg.miss_fill == "host":
+            return int(round(rows * 2 * cfg.d * HALF))
+        return int(round(rows * (2 * 2 * cfg.d * HALF + 8)))
+
+    def roofline_peak(self):
+        """(peak, source, bound) of the roofline kernel."""
+        if self.cfg.miss_fill == "host":
+            return measure_h2d_gbs(self.torch), "measured in this run: pinned host-to-device " \
+                "cudaMemcpyAsync of 512 MiB, best of 5", "c2c"
+        p, src = peak_hbm()
+        return p, src, "hbm"
 
     def launches_per_step(self) -> int:
         extra = (1 if self.restore is not None else 0) + (self.L if self.cfg.miss_fill else 0)
@@ -246,13 +278,14 @@ class HybridWorkload:
             return 1 + self.L * 2 + extra
         return 1 + self.L * (1 + self.attn_kernels) + extra
 
-    def _fill(self, step: int, l: int):
+    def _fill(self, step: int, l: int, events=None):
         """The miss path of layer l's lookup: its missed heads' rows from the
         full KV copy into the Cache Buffer (read on the device from the
         lookup's miss list)."""
         it = self.instance(step, l)
         self.clo.clo_fill_cache_buffer(it["srcK"], it["srcV"], it["idx"], None, it["cbK"],
-                                       it["cbV"], it["miss"], it["nmiss"], err_flag=self.err)
+                                       it["cbV"], it["miss"], it["nmiss"], err_flag=self.err,
+                                       num_ctas=self.fill_ctas, events=events)
 
     def _lookup(self, step: int, l: int):
         cfg = self.cfg
@@ -276,7 +309,7 @@ class HybridWorkload:
         it = self.instance(step, l)
         self.clo.clo_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"],
                                         it["pV"], it["pid"], it["out"], self.ws,
-                                        err_flag=self.err, events=events)
+                                        err_flag=self.err, num_ctas=self.main_ctas, events=events)
 
     def launch(self, step: int, attn_events=None):
         """One decode step.  With the "fused" schedule (the default) every
@@ -289,25 +322,33 @@ class HybridWorkload:
         layer l+1 starts when layer l starts (after attention l-1) and runs
         beside attention l, and the step's last lookup is the next step's
         layer 0 (replays of the step graph are ordered on the stream, so
-        attention 0 of a step always follows its lookup).  With the "serial"
-        schedule every layer runs lookup then attention on one stream."""
+        attention 0 of a step always follows its lookup).  With the "overlap"
+        schedule (for the miss-path fill) each layer first looks up layer l+1
+        on the main stream; the fill of layer l+1's missed heads then runs on
+        the second stream beside attention l, so the host-link transfer hides
+        behind this layer's attention (CLO section 3: the next layer's missed
+        heads move while the current layer computes), and attention l+1 waits
+        for it.  With the "serial" schedule every layer runs lookup (and fill)
+        then attention on one stream."""
         clo, cfg, torch = self.clo, self.cfg, self.torch
         if self.restore is not None:
             self.restore()
         if self.schedule == "fused":
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
             for l in range(self.L):
-                self._attention_lookup(step, l, None if attn_events is None else attn_events[l])
+                ev = None if attn_events is None else attn_events[l]
+                self._attention_lookup(step, l, None if cfg.miss_fill else ev)
                 if cfg.miss_fill:
-                    self._fill(step, l + 1)
+                    self._fill(step, l + 1, ev)
             return
         if self.schedule == "serial":
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
             for l in range(self.L):
+                ev = None if attn_events is None else attn_events[l]
                 self._lookup(step, l)
                 if cfg.miss_fill:
-                    self._fill(step, l)
-                self._attention(step, l, None if attn_events is None else attn_events[l])
+                    self._fill(step, l, ev)
+                self._attention(step, l, None if cfg.miss_fill else ev)
             return
         main = torch.cuda.current_stream()
         side = self.side
@@ -315,18 +356,38 @@ class HybridWorkload:
         fork.record(main)
         side.wait_event(fork)
         looked = [torch.cuda.Event() for _ in range(self.L + 1)]
+        if self.schedule == "overlap":
+            clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+            filled = [torch.cuda.Event() for _ in range(self.L + 1)]
+            for l in range(self.L):
+                ev = None if attn_events is None else attn_events[l]
+                self._lookup(step, l + 1)  # layer l+1; for l = L-1 the next step's layer 0
+                looked[l + 1].record(main)
+                with torch.cuda.stream(side):
+                    side.wait_event(looked[l + 1])
+                    if cfg.miss_fill:
+                        self._fill(step, l + 1, ev)
+                    filled[l + 1].record(side)
+                if l >= 1:
+                    main.wait_event(filled[l])
+                self._attention(step, l, None if cfg.miss_fill else ev)
+            main.wait_stream(side)  # the next step's layer 0 was filled in this step
+            return
         attn_done = [torch.cuda.Event() for _ in range(self.L)]
         with torch.cuda.stream(side):
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
         for l in range(self.L):
+            ev = None if attn_events is None else attn_events[l]
             with torch.cuda.stream(side):
                 if l >= 1:
                     side.wait_event(attn_done[l - 1])
                 self._lookup(step, l + 1)  # layer l+1; for l = L-1 the next step's layer 0
+                if cfg.miss_fill:
+                    self._fill(step, l + 1, ev)
                 looked[l + 1].record(side)
             if l >= 1:
                 main.wait_event(looked[l])
-            self._attention(step, l, None if attn_events is None else attn_events[l])
+            self._attention(step, l, None if cfg.miss_fill else ev)
             attn_done[l].record(main)
         main.wait_stream(side)
 
@@ -345,14 +406,21 @@ class HybridWorkload:
         self.h_io = self.io_all.cpu().pin_memory()
         self.e2e_h2d = self.q_all.numel() * HALF
         self.e2e_d2h = self.io_all.numel()
-        self.e2e_pipe = E2ECopies(clo, [(self.q_all, self.h_q)], [(self.h_io, self.io_all)])
+        ins = [(self.q_all, self.h_q)]
+        if self.restore is not None:  # the labels restored in the same copy launch
+            ins.append((self.lab_all, self.lab0_all))
+        self.e2e_pipe = E2ECopies(clo, ins, [(self.h_io, self.io_all)])
+        torch = self.torch
+        self.e2e_ev = [[torch.cuda.Event() for _ in range(self.L + 1)] for _ in range(3)]
         self.e2e_tau = clo.prepare_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
         self.e2e_layer = []
+        self.e2e_parts = []
         for j, it in enumerate(self.inst):
             def fill_of(x):
                 return (clo.prepare_fill_cache_buffer(x["srcK"], x["srcV"], x["idx"], None,
                                                       x["cbK"], x["cbV"], x["miss"], x["nmiss"],
-                                                      err_flag=self.err),) \
+                                                      err_flag=self.err,
+                                                      num_ctas=self.fill_ctas),) \
                     if cfg.miss_fill else ()
             if self.schedule == "fused":
                 # This layer's attention with the next layer's lookup.
@@ -366,18 +434,63 @@ class HybridWorkload:
                     fill_of(nx)
             else:
                 tau = self.tau[j * cfg.Hkv:(j + 1) * cfg.Hkv]
-                calls = (clo.prepare_lookup_update(it["q"], it["labels"], it["w"], tau,
-                                                   it["pmask"], it["flag"], it["sim"], it["miss"],
-                                                   it["nmiss"]),) + fill_of(it) + \
-                    (clo.prepare_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"],
-                                                    it["pK"], it["pV"], it["pid"], it["out"],
-                                                    self.ws, err_flag=self.err),)
+                look = (clo.prepare_lookup_update(it["q"], it["labels"], it["w"], tau,
+                                                  it["pmask"], it["flag"], it["sim"], it["miss"],
+                                                  it["nmiss"]),) + fill_of(it)
+                attn = (clo.prepare_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"],
+                                                       it["pK"], it["pV"], it["pid"], it["out"],
+                                                       self.ws, err_flag=self.err,
+                                                       num_ctas=self.main_ctas),)
+                self.e2e_parts.append((look, attn))
+                calls = look + attn
             self.e2e_layer.append(calls)
 
     def e2e_step(self, step: int):
-        self.e2e_pipe.step_in()
-        if self.restore is not None:
-            self.restore()
+        self.e2e_pipe.step_in()  # with label_reset this also restores the labels
+        if self.schedule == "overlap":  # the same two-stream order as launch()
+            torch = self.torch
+            main, side = torch.cuda.current_stream(), self.side
+            looked, filled, _ = self.e2e_ev
+            self.e2e_tau()
+            for l in range(self.L):
+                look = self.e2e_parts[(step * self.L + l + 1) % self.n_inst][0]
+                look[0]()  # the next layer's lookup, on the main stream
+                looked[l + 1].record(main)
+                with torch.cuda.stream(side):
+                    side.wait_event(looked[l + 1])
+                    for call in look[1:]:  # its fill, beside this layer's attention
+                        call()
+                    filled[l + 1].record(side)
+                if l >= 1:
+                    main.wait_event(filled[l])
+                for call in self.e2e_parts[(step * self.L + l) % self.n_inst][1]:
+                    call()
+            main.wait_stream(side)
+            return
+        if self.schedule == "stream":  # the same two-stream order as launch()
+            torch = self.torch
+            main, side = torch.cuda.current_stream(), self.side
+            looked, attn_done, fork_l = self.e2e_ev
+            fork = fork_l[0]
+            fork.record(main)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                self.e2e_tau()
+            for l in range(self.L):
+                look, _ = self.e2e_parts[(step * self.L + l + 1) % self.n_inst]
+                with torch.cuda.stream(side):
+                    if l >= 1:
+                        side.wait_event(attn_done[l - 1])
+                    for call in look:
+                        call()
+                    looked[l + 1].record(side)
+                if l >= 1:
+                    main.wait_event(looked[l])
+                for call in self.e2e_parts[(step * self.L + l) % self.n_inst][1]:
+                    call()
+                attn_done[l].record(main)
+            main.wait_stream(side)
+            return
         self.e2e_tau()
         for l in range(self.L):
             for call in self.e2e_layer[(step * self.L + l) % self.n_inst]:
@@ -438,8 +551,12 @@ class HybridWorkload:
                 "persistent_heads": c.Np, "cache_buffer": c.addressing,
                 "lookup_schedule": {
                     "fused": "next layer's lookup carried in each attention launch",
-                    "stream": "one layer ahead on a second stream",
+                    "stream": "one layer ahead on a second stream" + (
+                        ", the miss-path fill after it on that stream" if c.miss_fill else ""),
+                    "overlap": "one layer ahead on the main stream; the next layer's miss-path "
+                               "fill on a second stream beside this layer's attention",
                     "serial": "before each layer's attention, same stream"}[self.schedule],
+                "attention_ctas": self.main_ctas or "one full wave",
                 "physical_buffer_sets": self.n_inst,
                 "l2": f"inputs larger than L2: a buffer is re-read after "
                       f"{self.reuse_distance() / 2**30:.2f} GiB of other reads"} | (
@@ -974,7 +1091,8 @@ def run_ours(args):
             cfg = dataclasses.replace(cfg, B=args.batch)
         if args.ring and cfg.L > 1:
             cfg = dataclasses.replace(cfg, ring=args.ring)
-        W = HybridWorkload(cfg, dev, rank, args.replicas, schedule=args.lookup_schedule)
+        W = HybridWorkload(cfg, dev, rank, args.replicas, schedule=args.lookup_schedule,
+                           side_ctas=args.side_ctas)
     elif args.workload in wl.FILL_CONFIGS:
         W = FillWorkload(args.workload, dev, rank, args.batch)
     elif args.workload in wl.TOPK_CONFIGS:
@@ -1236,12 +1354,18 @@ def main(argv=None):
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--lookup-schedule", choices=["fused", "stream", "serial"], default="fused",
+    ap.add_argument("--lookup-schedule", choices=["fused", "stream", "serial", "overlap"],
+                    default="fused",
                     help="fused: the next layer's lookup rides in each attention launch; "
                          "stream: it runs one layer ahead on a second stream; serial: lookup "
-                         "then attention for every layer on one stream")
+                         "then attention for every layer on one stream; overlap: the next "
+                         "layer's lookup on the main stream, then its miss-path fill on a second "
+                         "stream beside this layer's attention")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases)")
+    ap.add_argument("--side-ctas", type=int, default=None,
+                    help="--lookup-schedule overlap: CTAs of the fill on the second stream (the "
+                         "attention grid leaves as many of its slots free)")
     ap.add_argument("--ring", type=int, default=0,
                     help="physical layer buffers of a multi-layer workload (0 = the workload's "
                          "own: one per layer, or its ring); smaller device footprints for "

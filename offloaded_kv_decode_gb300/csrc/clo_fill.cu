@@ -21,10 +21,15 @@
 namespace clo {
 
 constexpr int FILL_D = 128;  // head dimension (fp16 elements a row)
-constexpr int FILL_THREADS = 256;
+// 4-warp CTAs, 4 an SM: the same 16 warps an SM and register cap as larger
+// CTAs, and one fill CTA fits in the room of one attention CTA, so a fill
+// launched beside an attention grid that leaves a few CTA slots free runs
+// alongside it (a caller overlapping the next layer's fill with this layer's
+// attention).
+constexpr int FILL_THREADS = 128;
 constexpr int FILL_WARPS = FILL_THREADS / 32;
 constexpr int FILL_ROWS = 16;  // rows a warp moves per step
-constexpr int FILL_CTAS_PER_SM = 2;
+constexpr int FILL_CTAS_PER_SM = 4;
 
 struct FillParams {
     const clo_half* srcK;

@@ -1,6 +1,7 @@
 """bench.py end to end on small cases of every workload kind: the JSON line
 carries the contract's keys and sane values."""
 import contextlib
+import dataclasses
 import io
 import json
 
@@ -23,6 +24,10 @@ pytestmark = pytest.mark.gpu
     ["--workload", "llama3_8b_layer_b8_32k_miss", "--batch", "2"],
     ["--workload", "llama3_8b_layer_b8_32k_miss", "--batch", "2", "--lookup-schedule", "serial"],
     ["--workload", "llama3_8b_layer_b8_32k_miss_fill", "--batch", "1"],
+    ["--workload", "llama3_8b_layer_b8_32k_miss_fill", "--batch", "1", "--lookup-schedule",
+     "overlap"],
+    ["--workload", "llama3_8b_layer_b8_32k_miss_fill", "--batch", "1", "--lookup-schedule",
+     "stream"],
 ], ids=lambda a: "_".join(x.lstrip("-") for x in a[1::2] if x not in ("--batch",)))
 def test_bench_line(args):
     buf = io.StringIO()
@@ -44,3 +49,37 @@ def test_bench_line(args):
         # the misses recur every step (labels restored) and their bytes are counted
         assert d["config"]["misses_per_step"] > 0 and d["config"]["miss_bytes_per_step"] > 0
         assert 0.0 < d["lookup"]["hit_rate"] < 1.0
+
+
+def test_overlapped_fill_schedule_orders_the_fill_before_its_attention():
+    """The miss-path fill on the second stream (the next layer's fill beside
+    the current layer's attention, "overlap"; or lookup and fill there,
+    "stream") must leave every layer's attention output bit-identical to the
+    serial schedule's with the same CTA counts: an attention that ran before
+    its fill would read the old rows (the full KV copy holds other values
+    than the Cache Buffer)."""
+    import torch
+    import workloads as wl
+
+    cfg = dataclasses.replace(wl.CONFIGS["llama3_8b_layer_b8_32k_miss_fill"], B=1)
+    dev = torch.device("cuda:0")
+    outs = {}
+    for sched in ("serial", "overlap", "stream"):
+        W = bench.HybridWorkload(cfg, dev, 0, replicas=3, schedule=sched, side_ctas=32)
+        assert W.misses_per_step > 0
+        for i in range(2 * W.n_inst):  # every buffer set filled at least once
+            W.launch(i)
+        torch.cuda.synchronize()
+        for it in W.inst:
+            it["out"].fill_(float("nan"))
+        for i in range(2 * W.n_inst, 3 * W.n_inst):
+            W.launch(i)
+        torch.cuda.synchronize()
+        assert int(W.err.item()) == 0
+        outs[sched] = [it["out"].clone() for it in W.inst]
+        del W
+        torch.cuda.empty_cache()
+    for sched in ("overlap", "stream"):
+        for a, b in zip(outs["serial"], outs[sched]):
+            assert not torch.isnan(a).any()
+            assert torch.equal(a, b), sched
