@@ -235,7 +235,13 @@ typedef struct clo_attn_opts {
  *             outside [0, T) or a slot outside [0, C) sets CLO_FLAG_BAD_INDEX
  *             and that row (or head) is skipped; a count outside [0, B*Hkv]
  *             sets it and is clamped.
- * opts:       optional (see clo_attn_opts).
+ * opts:       optional (see clo_attn_opts).  num_ctas sets the fill's grid
+ *             (default: one wave of 4 CTAs an SM).  A fill CTA (4 warps, no
+ *             shared memory, at most 128 registers a thread) takes no more
+ *             room on an SM than an attention CTA, so a fill of N CTAs can run
+ *             on a second stream beside an attention launched with N fewer
+ *             CTAs than its default grid (3 an SM): the next layer's missed
+ *             rows then move while this layer's attention runs.
  * Requires d == 128; pointers to K/V 16-byte aligned.
  */
 clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int T,

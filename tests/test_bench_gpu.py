@@ -83,3 +83,36 @@ def test_overlapped_fill_schedule_orders_the_fill_before_its_attention():
         for a, b in zip(outs["serial"], outs[sched]):
             assert not torch.isnan(a).any()
             assert torch.equal(a, b), sched
+
+
+def test_overlapped_fill_schedule_across_layers():
+    """The same check on a three-layer step with a ring of five buffer sets
+    and the fill from a full KV copy in HBM: the attention of layer l+1 must
+    wait for the fill issued beside layer l, for every l, and for the next
+    step's layer 0."""
+    import torch
+    import workloads as wl
+
+    cfg = wl.small_hybrid("three_layers_miss_fill", B=3, L=3, Hq=32, Hkv=8, T=2048, Np=2,
+                          qmode="cos", c_lo=0.725, c_hi=0.925, smode="one", label_reset=True,
+                          miss_fill="device", ring=5, seed=4242)
+    dev = torch.device("cuda:0")
+    outs = {}
+    for sched in ("serial", "overlap"):
+        W = bench.HybridWorkload(cfg, dev, 0, schedule=sched, side_ctas=24)
+        assert W.n_inst == 5 and W.misses_per_step > 0
+        for i in range(4 * W.n_inst):
+            W.launch(i)
+        torch.cuda.synchronize()
+        for it in W.inst:
+            it["out"].fill_(float("nan"))
+        for i in range(4 * W.n_inst, 6 * W.n_inst):
+            W.launch(i)
+        torch.cuda.synchronize()
+        assert int(W.err.item()) == 0
+        outs[sched] = [it["out"].clone() for it in W.inst]
+        del W
+        torch.cuda.empty_cache()
+    for a, b in zip(outs["serial"], outs["overlap"]):
+        assert not torch.isnan(a).any()
+        assert torch.equal(a, b)
