@@ -244,7 +244,8 @@ class Oracle:
     def topk_retrieve(self, q, K, k: int) -> np.ndarray:
         """q [B][Hq][d], K [B][Hkv][T][d] fp16 -> idx int32 [B][Hkv][k]: per KV
         head the k tokens with the largest (sum of the group's q) . K_t,
-        ties to the lower token, ascending."""
+        ties to the lower token, ascending.  Not reentrant (the C sort's
+        comparator reads a file-level pointer): call it from one thread."""
         q, K = self._u16(q), self._u16(K)
         B, Hq, d = q.shape
         Hkv, T = K.shape[1], K.shape[2]

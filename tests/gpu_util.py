@@ -74,7 +74,8 @@ def assert_lookup_matches(ref, got, tau32, pm, G):
 
 def parallel_map(fn, items):
     """fn over items on the host cores (the oracle's C routines run outside
-    the GIL), results in input order."""
+    the GIL), results in input order.  For the oracle's attention and lookup
+    routines, which keep no state between calls; not for topk_retrieve."""
     items = list(items)
     workers = max(1, min(len(items), os.cpu_count() or 1))
     with ThreadPoolExecutor(max_workers=workers) as ex:

@@ -218,3 +218,14 @@ def test_fused_lookup_misses_full_step_shape():
     ref, got, near = fused_lookup_vs_oracle(cfg, s_next, 0, check_attn=False)
     print(f"B1 128K: {got['miss_count']} misses; {near} near tau")
 
+
+
+def test_fused_lookup_maximum_groups_vs_oracle():
+    """The carried lookup at its largest size, 65536 groups (8192 batch rows x
+    8 KV heads), beside an attention over the same batch (32-token contexts):
+    the merge launch then has 65536 blocks ahead of the lookup's cluster."""
+    cfg = wl.small_hybrid("max_groups", B=8192, Hq=32, Hkv=8, T=32, Np=2, qmode="cos",
+                          c_lo=0.5, c_hi=0.95, seed=9090)
+    s_next = _next_importance(cfg, "half_one", 11)
+    ref, got, near = fused_lookup_vs_oracle(cfg, s_next, 0)
+    print(f"65536 groups carried: {got['miss_count']} misses, {near} near tau")

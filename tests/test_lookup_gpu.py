@@ -128,3 +128,22 @@ def test_lookup_empty_batch():
                           mc)
     torch.cuda.synchronize()
     assert mc.item() == 0
+
+
+def test_lookup_maximum_groups():
+    """The largest lookup a call takes: 8192 batch rows x 8 KV heads = 65536
+    groups (one past it is refused on the host), about a third of them
+    missing, so each of the cluster's 8 CTAs writes thousands of misses at
+    offsets read from the others."""
+    rng = np.random.Generator(np.random.PCG64(65536))
+    B, Hq, Hkv = 8192, 32, 8
+    lab = rng.standard_normal((B, Hq, 128)).astype(np.float16)
+    q = (0.8 * lab.astype(np.float32) + 0.6 * rng.standard_normal((B, Hq, 128))).astype(np.float16)
+    w = rng.uniform(0, 1, Hq).astype(np.float32)
+    tau = np.array([0.79, 0.8, -1.0, 0.81, 0.8, 0.79, 0.5, 0.8], dtype=np.float32)
+    pm = np.zeros(Hkv, dtype=np.uint8)
+    pm[2] = 1
+    ref = oracle.get().lookup_update(q, lab, w.astype(np.float64), tau.astype(np.float64), pm)
+    assert B * Hkv // 5 < ref["miss_count"] < B * Hkv // 2
+    near = compare(q, lab, w, tau, pm)
+    print(f"65536 groups: {ref['miss_count']} misses, {near} near tau")
