@@ -65,7 +65,8 @@ typedef enum clo_status {
     CLO_ERR_UNSUPPORTED = 2,
     CLO_ERR_CUDA = 3,
     CLO_ERR_BAD_INDEX = 4,
-    CLO_ERR_WORKSPACE = 5
+    CLO_ERR_WORKSPACE = 5,
+    CLO_ERR_TIMEOUT = 6
 } clo_status;
 
 /* Bits a kernel ORs into *err_flag. */
@@ -73,6 +74,7 @@ typedef enum clo_status {
                                     miss-list entry, token or slot out of range */
 #define CLO_FLAG_BAD_PERSIST 0x2 /* persist_ids entry out of range or repeated */
 #define CLO_FLAG_BAD_CTX 0x4     /* a context length < 0 or > max_blocks*block_size */
+#define CLO_FLAG_TIMEOUT 0x8     /* clo_wait_ready gave up before the value arrived */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* clo_status_string(clo_status s);
@@ -81,7 +83,8 @@ const char* clo_status_string(clo_status s);
 int clo_version(void);
 
 /* Maps an err_flag value copied back to the host to a status: CLO_OK when
- * zero, CLO_ERR_BAD_INDEX when any CLO_FLAG_* bit is set. */
+ * zero, CLO_ERR_TIMEOUT when CLO_FLAG_TIMEOUT is set, else CLO_ERR_BAD_INDEX
+ * when any other CLO_FLAG_* bit is set. */
 clo_status clo_check_error_flag(int32_t host_err_flag);
 
 /* One copy of `bytes` bytes from src to dst. */
@@ -372,6 +375,44 @@ clo_status clo_hybrid_decode_attn_noalloc(const clo_half* q, const clo_half* cbK
 
 /* Size in bytes of the fixed scratch used by clo_hybrid_decode_attn_noalloc. */
 size_t clo_hybrid_noalloc_max_scratch(void);
+
+/*
+ * clo_wait_ready / clo_signal_ready -- GPU-centric data-ready synchronisation
+ * ("CLO: CPU-Light KVCache Offloading", section 2 Q1 "GPU-centric
+ * synchronisation" and Fig. 8's Data Synchronization Controller): the GPU
+ * polls a flag in host memory instead of the host blocking in
+ * cudaStreamSynchronize, so the thread that launches kernels can queue the
+ * work that needs some data before a host thread has finished moving it.
+ *
+ * clo_wait_ready queues on `stream` a one-warp kernel that waits until
+ * (int32_t)(*ready - expected) >= 0 (sequence numbers; wrap-around safe),
+ * then lets the work queued after it run.  The wait is bounded: after
+ * timeout_us microseconds (1 .. 10,000,000) it ORs CLO_FLAG_TIMEOUT into
+ * *err_flag (a caller-zeroed device int32; may be NULL) and returns, and the
+ * work after it runs on whatever the memory holds.  The caller reads the flag
+ * after the stream synchronises (clo_check_error_flag gives CLO_ERR_TIMEOUT).
+ *  - ready: 4-byte aligned memory the device reads in place: pinned host
+ *    memory (cudaHostAlloc, a pinned torch tensor; read through its mapped
+ *    address) or device memory.  Anything else gives CLO_ERR_INVALID_ARG.
+ *  - The value must be written by a host thread (clo_signal_ready), never by
+ *    another GPU kernel: kernels that wait on one another are not guaranteed
+ *    to run at the same time.
+ *  - The wait is an acquire at system scope: the data the host wrote before
+ *    clo_signal_ready published the value is visible to the kernels after it.
+ *  - Under lazy module loading (CUDA's default), the first launch of a kernel
+ *    in a process can wait for the device to go idle while its code loads.
+ *    Such a launch queued behind a wait that the launching thread's own later
+ *    work must release would stall until the wait runs out.  Launch every
+ *    kernel that follows a wait once beforehand (one call of each libclo
+ *    entry point loads its kernels), or set CUDA_MODULE_LOADING=EAGER.
+ *
+ * clo_signal_ready stores `value` to *ready (host memory) with release
+ * ordering, after a release fence: every earlier write of the calling thread
+ * is visible to a GPU that has seen the value.  Host code only; no GPU call.
+ */
+clo_status clo_wait_ready(const uint32_t* ready, uint32_t expected, uint32_t timeout_us,
+                          int32_t* err_flag, cudaStream_t stream);
+clo_status clo_signal_ready(uint32_t* ready, uint32_t value);
 
 /* Workspace bytes clo_paged_decode_attn needs (same rules as above). */
 size_t clo_paged_workspace_size(int B, int Hq, int Hkv, int d, int num_ctas);

@@ -28,10 +28,12 @@ CLO_ERR_UNSUPPORTED = 2
 CLO_ERR_CUDA = 3
 CLO_ERR_BAD_INDEX = 4
 CLO_ERR_WORKSPACE = 5
+CLO_ERR_TIMEOUT = 6
 
 FLAG_BAD_INDEX = 0x1
 FLAG_BAD_PERSIST = 0x2
 FLAG_BAD_CTX = 0x4
+FLAG_TIMEOUT = 0x8
 
 HEAD_DIM = 128
 
@@ -55,6 +57,8 @@ _SIGS = {
     "clo_version": ([], _I),
     "clo_check_error_flag": ([ctypes.c_int32], _I),
     "clo_copy_async": ([_P, _I, _P], _I),
+    "clo_wait_ready": ([_P, ctypes.c_uint32, ctypes.c_uint32, _P, _P], _I),
+    "clo_signal_ready": ([_P, ctypes.c_uint32], _I),
     "clo_thresholds": ([_P, _I, _I, _F, _F, _P, _P], _I),
     "clo_thresholds_host": ([_P, _I, _I, _F, _F, _P], _I),
     "clo_lookup_update": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
@@ -248,6 +252,36 @@ def prepare_copies(pairs: Sequence, stream=None) -> PreparedCall:
     """clo_copy_async on fixed buffers, checked once (see PreparedCall)."""
     what, args, keep = _copies_call(pairs)
     return PreparedCall(what, args, keep, stream)
+
+
+# ---------------------------------------------------------------- data-ready sync
+
+def _flag_ptr(ready: torch.Tensor) -> int:
+    if not isinstance(ready, torch.Tensor) or ready.dtype not in (torch.int32, torch.uint32) or \
+            ready.numel() < 1 or not ready.is_contiguous():
+        raise CloError("ready must be a contiguous 32-bit integer tensor", CLO_ERR_INVALID_ARG)
+    if not ready.is_cuda and not ready.is_pinned():
+        raise CloError("ready must be pinned host memory or a CUDA tensor", CLO_ERR_INVALID_ARG)
+    return ready.data_ptr()
+
+
+def clo_wait_ready(ready: torch.Tensor, expected: int, timeout_us: int,
+                   err_flag: Optional[torch.Tensor] = None, stream=None):
+    """Queues a bounded GPU wait until ready[0] reaches `expected` (sequence
+    numbers); on timeout FLAG_TIMEOUT is ORed into err_flag."""
+    pe = _dev(err_flag, "err_flag", torch.int32, optional=True)
+    _check(lib().clo_wait_ready(_flag_ptr(ready), int(expected) & 0xFFFFFFFF,
+                                int(timeout_us) & 0xFFFFFFFF, pe, _stream(stream)),
+           "clo_wait_ready")
+
+
+def clo_signal_ready(ready: torch.Tensor, value: int):
+    """Publishes `value` to ready[0] (pinned host memory) with release
+    ordering, from the calling host thread."""
+    if ready.is_cuda:
+        raise CloError("clo_signal_ready writes host memory", CLO_ERR_INVALID_ARG)
+    _check(lib().clo_signal_ready(_flag_ptr(ready), int(value) & 0xFFFFFFFF),
+           "clo_signal_ready")
 
 
 # ---------------------------------------------------------------- thresholds

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libclo.so")
 SOURCES = ["clo_api.cu", "clo_lookup.cu", "clo_attention.cu", "clo_fill.cu", "clo_plan.cu", "clo_topk.cu",
-           "clo_copy.cu"]
+           "clo_copy.cu", "clo_sync.cu"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 18, names
+    assert len(names) == 20, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -40,6 +40,9 @@ def test_status_helpers(L):
     assert clo.version() >= 100
     assert clo.check_error_flag(0) == clo.CLO_OK
     assert clo.check_error_flag(clo.FLAG_BAD_INDEX | clo.FLAG_BAD_PERSIST) == clo.CLO_ERR_BAD_INDEX
+    assert clo.check_error_flag(clo.FLAG_TIMEOUT) == clo.CLO_ERR_TIMEOUT
+    assert clo.check_error_flag(clo.FLAG_TIMEOUT | clo.FLAG_BAD_INDEX) == clo.CLO_ERR_TIMEOUT
+    assert clo.status_string(clo.CLO_ERR_TIMEOUT) == "CLO_ERR_TIMEOUT"
 
 
 def test_copy_async_validates_before_issuing(L):
@@ -250,3 +253,22 @@ def test_header_is_plain_c_and_links(L, tmp_path):
                                   5e9, 5e5)
     want = [ref["n_p"], int(ref["n_persist"][0])] + [int(x) for x in ref["persist_ids"][0][:3]]
     assert [int(x) for x in r.stdout.split()] == want, (r.stdout, want)
+
+
+def test_wait_ready_rejects_bad_arguments_and_signal_publishes(L):
+    """clo_wait_ready checks its arguments before touching the GPU (on this
+    machine every pointer is refused: no device can read it);
+    clo_signal_ready is host code and stores the value."""
+    import numpy as np
+
+    flag = np.zeros(4, dtype=np.uint32)
+    p = flag.ctypes.data
+    assert L.clo_wait_ready(None, 1, 1000, None, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_wait_ready(p + 2, 1, 1000, None, None) == clo.CLO_ERR_INVALID_ARG  # misaligned
+    assert L.clo_wait_ready(p, 1, 0, None, None) == clo.CLO_ERR_INVALID_ARG         # no limit
+    assert L.clo_wait_ready(p, 1, 10_000_001, None, None) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_wait_ready(p, 1, 1000, None, None) == clo.CLO_ERR_INVALID_ARG      # pageable
+    assert L.clo_signal_ready(None, 1) == clo.CLO_ERR_INVALID_ARG
+    assert L.clo_signal_ready(p, 0xFFFFFFF7) == clo.CLO_OK and flag[0] == 0xFFFFFFF7
+    assert L.clo_signal_ready(p + 4, 3) == clo.CLO_OK and flag[1] == 3
+
