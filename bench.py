@@ -202,10 +202,10 @@ class HybridWorkload:
         # "overlap": the next layer's fill runs on a second stream beside this
         # layer's attention.  The fill takes side_ctas CTAs (each fits in the
         # room of one attention CTA) and the attention grid leaves that many of
-        # its 3 x SMs slots free, so both are resident at once.  (None: 96 with
+        # its 3 x SMs slots free, so both are resident at once.  (None: 64 with
         # that schedule, else the full grids; a number applies to any schedule.)
         if side_ctas is None:
-            side_ctas = 96 if schedule == "overlap" else 0
+            side_ctas = 64 if schedule == "overlap" else 0
         self.side_ctas = side_ctas
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.main_ctas = max(1, 3 * sms - self.side_ctas) if self.side_ctas else 0

@@ -131,6 +131,16 @@ CONFIGS = {
         "llama3_8b_layer_b8_32k_miss_fill", B=8, L=1, Hq=32, Hkv=8, T=32768, Np=2,
         qmode="cos", c_lo=0.725, c_hi=0.925, smode="one", label_reset=True,
         miss_fill="host", seed=1239),
+    # The batch-1, 128K-context step (the page's single-layer setting: Llama3-8B,
+    # BSZ 1, 128K, top-k 10%) with misses at the page's hit rate and the missed
+    # heads' rows fetched from a full KV copy in pinned host memory.  Every
+    # layer has its own buffers (17 GB of pinned host memory for the full
+    # copies): the same heads miss every step, and with fewer physical layers
+    # their rows would be read from L2, not over the host link.
+    "llama3_8b_step_b1_128k_miss_fill": HybridConfig(
+        "llama3_8b_step_b1_128k_miss_fill", B=1, L=32, Hq=32, Hkv=8, T=131072, Np=2,
+        qmode="cos", c_lo=0.725, c_hi=0.925, smode="one", label_reset=True,
+        miss_fill="host", seed=1240),
     # Qwen2.5-14B-shaped decode step: 48 layers, GQA 5, batch 16, context 64K,
     # 15% of heads with cosine ~0.6; a ring of 8 physical layer buffers.
     "qwen25_14b_step_b16_64k": HybridConfig(
