@@ -195,3 +195,64 @@ def test_peaked_softmax(gain):
         # lse grows with the gain; hold it to the same relative precision
         err = np.abs(lse.cpu().numpy() - ref_lse)
         assert np.all(err < LSE_ATOL * np.maximum(1.0, np.abs(ref_lse))), f"gain {gain}"
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_fused_lookup_random_shape(i):
+    """clo_hybrid_decode_attn_lookup on a random shape: the attention against
+    the oracle's, and the carried lookup (about half the KV heads at s = 1, so
+    tau = eta and some groups miss) against oracle_lookup_update bit for bit."""
+    from gpu_util import assert_lookup_matches
+
+    B, Hq, Hkv, T, k, Np, C, num_ctas = _hybrid_shape(500 + i)
+    G = Hq // Hkv
+    r = np.random.Generator(np.random.PCG64(3000 + i))
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    q = f16(B, Hq, 128)
+    cbK, cbV = f16(B, Hkv, C, 128), f16(B, Hkv, C, 128)
+    idx = np.stack([np.stack([r.permutation(C)[:k] for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    pK, pV = f16(B, Np, T, 128), f16(B, Np, T, 128)
+    pid = r.permutation(Hkv)[:Np].astype(np.int32)
+    # The next layer's lookup inputs.
+    lab = r.standard_normal((B, Hq, 128))
+    qn = (0.8 * lab + 0.6 * r.standard_normal((B, Hq, 128))).astype(np.float16)
+    lab = lab.astype(np.float16)
+    s = r.uniform(0, 1, Hq).astype(np.float32)
+    for g in range(Hkv):
+        if r.integers(0, 2):
+            s[g * G:(g + 1) * G] = 1.0
+    tau = clo.clo_thresholds_host(s, Hkv, G)
+    pm = np.zeros(Hkv, dtype=np.uint8)
+    pm[r.permutation(Hkv)[:int(r.integers(0, Hkv + 1))]] = 1
+    ref, ref_lse = oracle.get().hybrid_attn(q, cbK, cbV, idx, pK, pV, pid, scale_for())
+    ref_lk = oracle.get().lookup_update(qn, lab, s.astype(np.float64), tau.astype(np.float64), pm)
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    d = dev()
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=d)
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=d)
+    ws = torch.empty(clo.clo_hybrid_workspace_size(B, Hq, Hkv, 128, num_ctas), dtype=torch.uint8,
+                     device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    labd = t(lab)
+    n = B * Hkv
+    flag = torch.full((n,), 9, dtype=torch.uint8, device=d)
+    sim = torch.full((n,), -9.0, device=d)
+    miss = torch.full((n,), -9, dtype=torch.int32, device=d)
+    cnt = torch.full((1,), -9, dtype=torch.int32, device=d)
+    has_cb = Np < Hkv
+    clo.clo_hybrid_decode_attn_lookup(
+        t(q), t(cbK) if has_cb else None, t(cbV) if has_cb else None, t(idx) if has_cb else None,
+        t(pK) if Np else None, t(pV) if Np else None, t(pid) if Np else None, out, ws,
+        t(qn), labd, t(s), t(tau), t(pm), flag, sim, miss, cnt, lse=lse, err_flag=err,
+        num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    what = f"case {i}: B{B} Hq{Hq} Hkv{Hkv} T{T} k{k} Np{Np} C{C} ctas{num_ctas}"
+    assert_close(out.cpu().numpy(), ref, what)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) < LSE_ATOL
+    m = int(cnt.item())
+    got = dict(flag=flag.cpu().numpy(), sim=sim.cpu().numpy(), labels=labd.cpu().numpy(),
+               miss_list=miss.cpu().numpy()[:max(m, 0)], miss_count=m)
+    assert_lookup_matches(ref_lk, got, tau, pm, G)
