@@ -238,6 +238,10 @@ def test_header_is_plain_c_and_links(L, tmp_path):
         "    float s3[3] = {1.0f, 0.0f, 0.5f}, t3[3];\n"
         "    if (clo_thresholds_host(s3, 3, 1, 0.8f, 3.0f, t3) != CLO_OK) return 7;\n"
         "    if (t3[0] < 0.799999f || t3[0] > 0.800001f || t3[1] > -0.999999f) return 8;\n"
+        "    /* the host side of the data-ready sync */\n"
+        "    uint32_t ready = 0;\n"
+        "    if (clo_signal_ready(&ready, 42u) != CLO_OK || ready != 42u) return 9;\n"
+        "    if (clo_wait_ready(&ready, 42u, 0u, NULL, 0) != CLO_ERR_INVALID_ARG) return 10;\n"
         '    printf("%d %d %d %d %d\\n", np_, npers[0], ids[0], ids[1], ids[2]);\n'
         "    return 0;\n}\n")
     exe = tmp_path / "use_clo"
