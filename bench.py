@@ -205,7 +205,8 @@ class HybridWorkload:
         # its 3 x SMs slots free, so both are resident at once.  (None: 64 with
         # that schedule, else the full grids; a number applies to any schedule.)
         if side_ctas is None:
-            side_ctas = 64 if schedule == "overlap" else 0
+            side_ctas = 64 if schedule == "overlap" or (schedule == "pipelined" and
+                                                          cfg.miss_fill) else 0
         self.side_ctas = side_ctas
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.main_ctas = max(1, 3 * sms - self.side_ctas) if self.side_ctas else 0
@@ -218,6 +219,15 @@ class HybridWorkload:
             # The fill moves the step's rows over the host link (or reads and
             # writes them in HBM): the roofline line covers it.
             self.kernel, self.kernel_src = "fill_kernel", "clo_fill.cu"
+            if schedule == "pipelined":
+                # Carried beside the attention in the layer call, the fill is
+                # timed by the call's events, which bracket both kernels.
+                self.kernel = "fill_beside_kernel"
+                self.launch_ms_source = (
+                    "CUDA events around each layer call (the attention's main kernel and the "
+                    "fill beside it) in a second copy of the step graph, replayed after each "
+                    "timed round; the fill starts just after the main kernel's CTAs and ends "
+                    "last, so the bracket is an upper bound on its duration")
 
     def _count_misses(self) -> float:
         """Misses of one step's L lookups, averaged over the buffer sets (one
@@ -274,7 +284,7 @@ class HybridWorkload:
 
     def launches_per_step(self) -> int:
         extra = (1 if self.restore is not None else 0) + (self.L if self.cfg.miss_fill else 0)
-        if self.schedule == "fused":  # main kernel + merge launch carrying the lookup
+        if self.schedule in ("fused", "pipelined"):  # main kernel + merge launch (+ lookup)
             return 1 + self.L * 2 + extra
         return 1 + self.L * (1 + self.attn_kernels) + extra
 
@@ -305,6 +315,28 @@ class HybridWorkload:
             self.ws, nx["q"], nx["labels"], nx["w"], tau, nx["pmask"], nx["flag"], nx["sim"],
             nx["miss"], nx["nmiss"], err_flag=self.err, events=events)
 
+    def _layer_args(self, j: int) -> dict:
+        """clo_hybrid_decode_layer keyword arguments for buffer set j: its
+        attention, the fill of set j + 1 (with the miss-path fill; its miss
+        list came from an earlier call's lookup) and the lookup of set j + 2."""
+        cfg = self.cfg
+        it = self.inst[j % self.n_inst]
+        fl = self.inst[(j + 1) % self.n_inst]
+        j2 = (j + 2) % self.n_inst
+        nx = self.inst[j2]
+        tau = self.tau[j2 * cfg.Hkv:(j2 + 1) * cfg.Hkv]
+        fill = (fl["srcK"], fl["srcV"], fl["idx"], None, fl["cbK"], fl["cbV"], fl["miss"],
+                fl["nmiss"]) if cfg.miss_fill else None
+        return dict(q=it["q"], cbK=it["cbK"], cbV=it["cbV"], idx=it["idx"], pK=it["pK"],
+                    pV=it["pV"], persist_ids=it["pid"], out=it["out"], workspace=self.ws,
+                    fill=fill,
+                    lookup=(nx["q"], nx["labels"], nx["w"], tau, nx["pmask"], nx["flag"],
+                            nx["sim"], nx["miss"], nx["nmiss"]),
+                    err_flag=self.err, num_ctas=self.main_ctas, fill_ctas=self.fill_ctas)
+
+    def _layer(self, step: int, l: int, events=None):
+        self.clo.clo_hybrid_decode_layer(**self._layer_args(step * self.L + l), events=events)
+
     def _attention(self, step: int, l: int, events=None):
         it = self.instance(step, l)
         self.clo.clo_hybrid_decode_attn(it["q"], it["cbK"], it["cbV"], it["idx"], it["pK"],
@@ -328,8 +360,15 @@ class HybridWorkload:
         the second stream beside attention l, so the host-link transfer hides
         behind this layer's attention (CLO section 3: the next layer's missed
         heads move while the current layer computes), and attention l+1 waits
-        for it.  With the "serial" schedule every layer runs lookup (and fill)
-        then attention on one stream."""
+        for it.  With the "pipelined" schedule every layer is one
+        clo_hybrid_decode_layer call on one stream: the attention of layer l,
+        the fill of layer l+1 beside it (its CTAs in slots the attention grid
+        leaves free) and the lookup of layer l+2 in its merge launch, so each
+        layer's lookup runs a layer of compute ahead of the attention before
+        it, and its fill beside that attention (CLO section 3 Fig. 9); the
+        step's last two calls fill and look up the next step's first layers.
+        With the "serial" schedule every layer runs lookup (and fill) then
+        attention on one stream."""
         clo, cfg, torch = self.clo, self.cfg, self.torch
         if self.restore is not None:
             self.restore()
@@ -340,6 +379,11 @@ class HybridWorkload:
                 self._attention_lookup(step, l, None if cfg.miss_fill else ev)
                 if cfg.miss_fill:
                     self._fill(step, l + 1, ev)
+            return
+        if self.schedule == "pipelined":
+            clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
+            for l in range(self.L):
+                self._layer(step, l, None if attn_events is None else attn_events[l])
             return
         if self.schedule == "serial":
             clo.clo_thresholds(self.s, self.tau, cfg.G, wl.ETA, wl.N_EXP)
@@ -422,7 +466,9 @@ class HybridWorkload:
                                                       err_flag=self.err,
                                                       num_ctas=self.fill_ctas),) \
                     if cfg.miss_fill else ()
-            if self.schedule == "fused":
+            if self.schedule == "pipelined":
+                calls = (clo.prepare_hybrid_decode_layer(**self._layer_args(j)),)
+            elif self.schedule == "fused":
                 # This layer's attention with the next layer's lookup.
                 jn = (j + 1) % self.n_inst
                 nx = self.inst[jn]
@@ -555,7 +601,10 @@ class HybridWorkload:
                         ", the miss-path fill after it on that stream" if c.miss_fill else ""),
                     "overlap": "one layer ahead on the main stream; the next layer's miss-path "
                                "fill on a second stream beside this layer's attention",
-                    "serial": "before each layer's attention, same stream"}[self.schedule],
+                    "serial": "before each layer's attention, same stream",
+                    "pipelined": "one call a layer on one stream: attention l, the miss-path "
+                                 "fill of layer l+1 beside it, the lookup of layer l+2 in its "
+                                 "merge launch"}[self.schedule],
                 "attention_ctas": self.main_ctas or "one full wave",
                 "physical_buffer_sets": self.n_inst,
                 "l2": f"inputs larger than L2: a buffer is re-read after "
@@ -1301,12 +1350,12 @@ def run_ours(args):
                      "kernel": kernel, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": W.attn_bytes_per_launch(),
                      "launch_ms_mean": attn_ms_mean, "launch_samples": len(attn_ms),
-                     "launch_ms_source": "CUDA events recorded around the kernel in a second copy "
-                                         "of the step graph, replayed after each timed round; "
-                                         "the event nodes serialise the launches next to the "
-                                         "kernel (no programmatic overlap), so the duration is "
-                                         "a little longer than the kernel's share of a chained "
-                                         "step",
+                     "launch_ms_source": getattr(
+                         W, "launch_ms_source",
+                         "CUDA events recorded around the kernel in a second copy of the step "
+                         "graph, replayed after each timed round; the event nodes serialise the "
+                         "launches next to the kernel (no programmatic overlap), so the duration "
+                         "is a little longer than the kernel's share of a chained step"),
                      "layer_step_ms": ms_step / W.L},
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -1382,18 +1431,22 @@ def main(argv=None):
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--lookup-schedule", choices=["fused", "stream", "serial", "overlap"],
+    ap.add_argument("--lookup-schedule",
+                    choices=["fused", "stream", "serial", "overlap", "pipelined"],
                     default="fused",
                     help="fused: the next layer's lookup rides in each attention launch; "
                          "stream: it runs one layer ahead on a second stream; serial: lookup "
                          "then attention for every layer on one stream; overlap: the next "
                          "layer's lookup on the main stream, then its miss-path fill on a second "
-                         "stream beside this layer's attention")
+                         "stream beside this layer's attention; pipelined: one "
+                         "clo_hybrid_decode_layer call a layer on one stream (attention l, the "
+                         "fill of layer l+1 beside it, the lookup of layer l+2 in its merge "
+                         "launch)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--side-ctas", type=int, default=None,
-                    help="--lookup-schedule overlap: CTAs of the fill on the second stream (the "
-                         "attention grid leaves as many of its slots free)")
+                    help="--lookup-schedule overlap or pipelined: CTAs of the fill beside the "
+                         "attention (the attention grid leaves as many of its slots free)")
     ap.add_argument("--ring", type=int, default=0,
                     help="physical layer buffers of a multi-layer workload (0 = the workload's "
                          "own: one per layer, or its ring); smaller device footprints for "

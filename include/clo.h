@@ -342,6 +342,73 @@ clo_status clo_hybrid_decode_attn_lookup(
     uint8_t* flag_next, float* sim_next, int32_t* miss_list_next, int32_t* miss_count_next,
     const clo_attn_opts* opts, cudaStream_t stream);
 
+/* The next layer's miss-path fill carried by clo_hybrid_decode_layer.  Fields
+ * as the arguments of clo_fill_cache_buffer with the same names (the batch,
+ * KV heads and head dimension are the layer call's B, Hkv and d). */
+typedef struct clo_fill_args {
+    const clo_half* srcK;
+    const clo_half* srcV;
+    int T;
+    const int32_t* tok;
+    const int32_t* slot;
+    int k;
+    clo_half* cbK;
+    clo_half* cbV;
+    int C;
+    const int32_t* miss_list;
+    const int32_t* miss_count;
+    int num_ctas; /* CTAs of the fill; 0 = one in seven of the default attention grid's slots,
+                     at most as many as the longest possible miss list keeps busy */
+} clo_fill_args;
+
+/* A lookup carried by clo_hybrid_decode_layer.  Fields as the arguments of
+ * clo_lookup_update with the same names (tau = tau_kv; B, Hq, Hkv and d are
+ * the layer call's). */
+typedef struct clo_lookup_args {
+    const clo_half* q;
+    clo_half* labels;
+    const float* w_q;
+    const float* tau;
+    const uint8_t* persist_mask;
+    uint8_t* flag;
+    float* sim;
+    int32_t* miss_list;
+    int32_t* miss_count;
+} clo_lookup_args;
+
+/*
+ * clo_hybrid_decode_layer -- one layer of CLO's decode flow as one call on
+ * one stream (CLO section 3, Fig. 9: the lookup for a layer runs a layer
+ * ahead of its attention, with an approximate query, and the missed heads'
+ * rows move while the layer before it computes).  For layer l it runs
+ *   - clo_hybrid_decode_attn of layer l (the arguments up to err_flag);
+ *   - fill (may be NULL): clo_fill_cache_buffer for layer l+1, whose miss list
+ *     an earlier call's lookup wrote.  Its CTAs run beside the attention's
+ *     main kernel in CTA slots that grid leaves free: with opts->num_ctas == 0
+ *     the attention takes the default grid less fill->num_ctas CTAs (less the
+ *     fill's default share when that is 0);
+ *   - lookup (may be NULL): clo_lookup_update for layer l+2, carried by the
+ *     attention's merge launch as in clo_hybrid_decode_attn_lookup.
+ * Called for l = 0, 1, ... this gives each layer's lookup one layer of
+ * compute ahead of the layer's attention, and its fill the whole attention of
+ * the layer before.  The results are those of the three calls made
+ * separately, in any order, so the three must touch disjoint memory: the
+ * fill's Cache Buffer is not the one the attention reads, and its miss list
+ * and count are not the ones the lookup writes (both checked by pointer:
+ * CLO_ERR_INVALID_ARG), and the lookup's labels and outputs are not read by
+ * the other two.  The fill reports bad rows in err_flag, like the attention.
+ * opts: num_ctas as for clo_hybrid_decode_attn; ev_begin is recorded before
+ * the attention's main kernel, ev_end after the fill (after the main kernel
+ * when there is none), so the two bracket both kernels.  The workspace size
+ * for num_ctas == 0 is enough with or without a fill.
+ */
+clo_status clo_hybrid_decode_layer(
+    const clo_half* q, const clo_half* cbK, const clo_half* cbV, const int32_t* idx, int k, int C,
+    const clo_half* pK, const clo_half* pV, const int32_t* persist_ids, int Np, int T, int B,
+    int Hq, int Hkv, int d, float scale, clo_half* out, float* lse, void* workspace,
+    size_t ws_bytes, int32_t* err_flag, const clo_fill_args* fill, const clo_lookup_args* lookup,
+    const clo_attn_opts* opts, cudaStream_t stream);
+
 /*
  * clo_hybrid_decode_attn_noalloc -- clo_hybrid_decode_attn for callers that
  * cannot allocate device memory: serving engines that reserve all free device

@@ -77,6 +77,8 @@ _SIGS = {
     "clo_hybrid_decode_attn_lookup": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                        _F, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P], _I),
+    "clo_hybrid_decode_layer": ([_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                 _F, _P, _P, _P, _SZ, _P, _P, _P, _P, _P], _I),
     "clo_paged_workspace_size": ([_I, _I, _I, _I, _I], _SZ),
     "clo_paged_decode_attn": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                _P, _SZ, _P, _P, _P], _I),
@@ -456,6 +458,15 @@ def prepare_fill_cache_buffer(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_c
 
 def _fill_call(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag, num_ctas,
                events):
+    a = _fill_args(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count)
+    pe = _dev(err_flag, "err_flag", torch.int32, optional=True)
+    opts = _opts(num_ctas, events)
+    return ("clo_fill_cache_buffer",
+            a + (pe, None if opts is None else ctypes.byref(opts)),
+            (srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag, opts))
+
+
+def _fill_args(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count):
     ps = _dev_or_pinned(srcK, "srcK", torch.float16, 4)
     pv = _dev_or_pinned(srcV, "srcV", torch.float16, 4)
     B, Hkv, T, d = srcK.shape
@@ -472,12 +483,7 @@ def _fill_call(srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag,
         raise CloError("fill shapes do not match", CLO_ERR_INVALID_ARG)
     pml = _dev(miss_list, "miss_list", torch.int32)
     pmc = _dev(miss_count, "miss_count", torch.int32)
-    pe = _dev(err_flag, "err_flag", torch.int32, optional=True)
-    opts = _opts(num_ctas, events)
-    return ("clo_fill_cache_buffer",
-            (ps, pv, T, pt, psl, k, pk, pcv, C, pml, pmc, B, Hkv, d, pe,
-             None if opts is None else ctypes.byref(opts)),
-            (srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count, err_flag, opts))
+    return (ps, pv, T, pt, psl, k, pk, pcv, C, pml, pmc, B, Hkv, d)
 
 
 # ---------------------------------------------------------------- attention
@@ -569,6 +575,77 @@ def _hybrid_lookup_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, q
             (q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, q_next, labels_next, w_q_next,
              tau_next, persist_mask_next, flag_next, sim_next, miss_list_next, miss_count_next,
              lse, err_flag, opts))
+
+
+class FillArgs(ctypes.Structure):
+    _fields_ = [("srcK", ctypes.c_void_p), ("srcV", ctypes.c_void_p), ("T", ctypes.c_int),
+                ("tok", ctypes.c_void_p), ("slot", ctypes.c_void_p), ("k", ctypes.c_int),
+                ("cbK", ctypes.c_void_p), ("cbV", ctypes.c_void_p), ("C", ctypes.c_int),
+                ("miss_list", ctypes.c_void_p), ("miss_count", ctypes.c_void_p),
+                ("num_ctas", ctypes.c_int)]
+
+
+class LookupArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("labels", ctypes.c_void_p), ("w_q", ctypes.c_void_p),
+                ("tau", ctypes.c_void_p), ("persist_mask", ctypes.c_void_p),
+                ("flag", ctypes.c_void_p), ("sim", ctypes.c_void_p),
+                ("miss_list", ctypes.c_void_p), ("miss_count", ctypes.c_void_p)]
+
+
+def clo_hybrid_decode_layer(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, fill=None,
+                            lookup=None, lse=None, err_flag=None, scale=None, num_ctas: int = 0,
+                            fill_ctas: int = 0, events=None, stream=None):
+    """One layer of the decode flow on one stream: clo_hybrid_decode_attn for
+    this layer, the next layer's fill beside it and a later layer's lookup in
+    its merge launch.
+
+    fill: None or the tensors of clo_fill_cache_buffer, (srcK, srcV, tok,
+    slot, cbK, cbV, miss_list, miss_count), for the next layer; fill_ctas its
+    CTAs (0: the library's share).  lookup: None or the tensors of
+    clo_lookup_update, (q, labels, w_q, tau_kv, persist_mask, flag, sim,
+    miss_list, miss_count), for the layer after.  The results equal the
+    separate calls; the three must use disjoint buffers."""
+    _run(_layer_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, fill, lookup, lse,
+                     err_flag, scale, num_ctas, fill_ctas, events), stream)
+
+
+def prepare_hybrid_decode_layer(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace,
+                                fill=None, lookup=None, lse=None, err_flag=None, scale=None,
+                                num_ctas: int = 0, fill_ctas: int = 0, events=None,
+                                stream=None) -> PreparedCall:
+    """clo_hybrid_decode_layer on fixed buffers, checked once (see PreparedCall)."""
+    return PreparedCall(*_layer_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, fill,
+                                     lookup, lse, err_flag, scale, num_ctas, fill_ctas, events),
+                        stream)
+
+
+def _layer_call(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, fill, lookup, lse,
+                err_flag, scale, num_ctas, fill_ctas, events):
+    a = _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale)
+    fa = la = None
+    if fill is not None:
+        if len(fill) != 8:
+            raise CloError("fill: (srcK, srcV, tok, slot, cbK, cbV, miss_list, miss_count)",
+                           CLO_ERR_INVALID_ARG)
+        f = _fill_args(*fill)
+        if (f[11], f[12], f[13]) != (a[11], a[13], a[14]):
+            raise CloError("the fill must have this layer's B, Hkv, d", CLO_ERR_INVALID_ARG)
+        fa = FillArgs(f[0], f[1], f[2], f[3], f[4] or None, f[5], f[6], f[7], f[8], f[9], f[10],
+                      int(fill_ctas))
+    if lookup is not None:
+        if len(lookup) != 9:
+            raise CloError("lookup: (q, labels, w_q, tau_kv, persist_mask, flag, sim, "
+                           "miss_list, miss_count)", CLO_ERR_INVALID_ARG)
+        b = _lookup_args(*lookup)
+        if b[5:9] != a[11:15]:
+            raise CloError("the lookup must have this layer's B, Hq, Hkv, d", CLO_ERR_INVALID_ARG)
+        la = LookupArgs(b[0], b[1], b[2], b[3], b[4] or None, b[9], b[10], b[11], b[12])
+    opts = _opts(num_ctas, events)
+    return ("clo_hybrid_decode_layer",
+            a + (None if fa is None else ctypes.byref(fa), None if la is None else ctypes.byref(la),
+                 None if opts is None else ctypes.byref(opts)),
+            (q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, fill, lookup, lse, err_flag,
+             fa, la, opts))
 
 
 def _hybrid_args(q, cbK, cbV, idx, pK, pV, persist_ids, out, workspace, lse, err_flag, scale):

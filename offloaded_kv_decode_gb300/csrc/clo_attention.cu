@@ -49,6 +49,7 @@
 #include <mutex>
 
 #include "clo_device.cuh"
+#include "clo_fill.cuh"
 #include "clo_lookup.cuh"
 
 namespace clo {
@@ -91,6 +92,11 @@ constexpr int MAX_ROWS = 1 << 24;  // rows per head: row offsets stay 32-bit
 constexpr int SMEM_LIMIT = 227 * 1024;     // per CTA
 constexpr int SMEM_PER_SM = 228 * 1024;    // per SM, 1 KB of it reserved per resident CTA
 constexpr int MERGE_SMEM_LIMIT = 96 * 1024;
+// Default share of the main kernel's CTA slots given to a fill carried beside
+// it: one in FILL_SHARE (65 of 456 on 152 SMs).  On the B8 32K layer and the
+// B1 128K step, with misses fetched over the host link, 48 to 96 fill CTAs
+// were within 2% of the best step time.
+constexpr int FILL_SHARE = 7;
 
 // One token set: batch row (or request) b, KV head kv.
 struct Seg {
@@ -959,6 +965,7 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
             __shared__ int lk_misses;
             lookup_cluster<MERGE_THREADS / 32>(lk, msmem, &lk_misses);
         }
+        if (blockIdx.x == 0 && blockIdx.y == 0) pdl_wait();  // see below
         return;
     }
     // Static layouts (hybrid): block s handles token set s if CTA boundaries
@@ -978,7 +985,16 @@ __global__ void __launch_bounds__(MERGE_THREADS, 1)
         const long long last = first + geo.segment_ntiles(s) - 1;
         c_lo = static_cast<int>(((first + 1) * Ce - 1) / N);
         const int c_hi = static_cast<int>(((last + 1) * Ce - 1) / N);
-        if (c_lo == c_hi) return;
+        // Block (0, 0) waits for the grid ahead even with nothing to merge
+        // (as do the blocks that merge), so this grid never finishes before
+        // that grid, nor, through that grid's own wait, before any kernel
+        // further back: the next kernel, which waits for this grid alone,
+        // finds all of them finished.  (A fill launched beside the main
+        // kernel relies on it: the next layer's attention reads its rows.)
+        if (c_lo == c_hi) {
+            if (blockIdx.x == 0 && blockIdx.y == 0) pdl_wait();
+            return;
+        }
         P = c_hi - c_lo + 1;
         pdl_wait();
     } else {
@@ -1185,11 +1201,14 @@ static size_t merge_smem_bytes(int /*G*/, size_t geo_ints) {
            static_cast<size_t>(2) * MERGE_THREADS * sizeof(float4) + geo_ints * sizeof(int);
 }
 
+// Launches the main kernel, then (if given) a fill beside it, then the merge
+// launch (carrying the lookup, if given).
 template <class Geo>
 static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_host_bound,
                                    size_t geo_ints, int S, void* workspace, size_t ws_bytes,
                                    const clo_attn_opts* opts, cudaStream_t stream,
-                                   const LookupParams* lookup = nullptr) {
+                                   const LookupParams* lookup = nullptr,
+                                   const FillParams* fill = nullptr, int fill_ctas = 0) {
     if (!prepare_kernel(reinterpret_cast<const void*>(attn_split_kernel<Geo>), SMEM_LIMIT) ||
         !prepare_kernel(reinterpret_cast<const void*>(attn_merge_kernel<Geo>), MERGE_SMEM_LIMIT))
         return CLO_ERR_CUDA;
@@ -1203,8 +1222,21 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
     int per_sm = static_cast<int>(SMEM_PER_SM / (smem + 1024));
     if (per_sm > ATTN_CTAS_PER_SM) per_sm = ATTN_CTAS_PER_SM;
     if (per_sm < 1) return CLO_ERR_UNSUPPORTED;
-    int C = (opts != nullptr && opts->num_ctas > 0) ? opts->num_ctas : device_sm_count() * per_sm;
-    if (C <= 0) return CLO_ERR_CUDA;
+    const int wave = device_sm_count() * per_sm;
+    if (wave <= 0) return CLO_ERR_CUDA;
+    // A fill carried beside the main kernel runs in CTA slots the main grid
+    // leaves free (a fill CTA fits in the room of one main-kernel CTA): by
+    // default one slot in FILL_SHARE, never more CTAs than the largest fill
+    // can use.
+    long long fill_grid = 0;
+    if (fill != nullptr) {
+        fill_grid = fill_ctas > 0 ? fill_ctas
+                                  : std::min(std::max(wave / FILL_SHARE, 1), static_cast<int>(fill_max_grid(*fill)));
+        if (fill_grid <= 0) return CLO_ERR_CUDA;
+    }
+    int C = (opts != nullptr && opts->num_ctas > 0)
+                ? opts->num_ctas
+                : static_cast<int>(std::max(wave - fill_grid, 1ll));
     // Never more CTAs than tiles (no CTA gets an empty range) and at least one
     // tile per warp where the problem allows.
     const long long cap = n_tiles_host_bound / ATTN_WARPS;
@@ -1222,6 +1254,12 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
         return CLO_ERR_CUDA;
     if (launch_pdl(attn_split_kernel<Geo>, dim3(C), dim3(ATTN_THREADS), smem, stream, geo, o) !=
         cudaSuccess)
+        return CLO_ERR_CUDA;
+    // The fill starts as soon as every main-kernel CTA has passed its
+    // dependency wait and runs beside them; the merge launch below waits for
+    // the fill, which waits for the main kernel at its end.
+    if (fill != nullptr &&
+        launch_fill(*fill, static_cast<int>(fill_grid), true, stream) != cudaSuccess)
         return CLO_ERR_CUDA;
     if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
@@ -1274,7 +1312,8 @@ static clo_status hybrid_attention(const clo_half* q, const clo_half* cbK, const
                                    int B, int Hq, int Hkv, int d, float scale, clo_half* out,
                                    float* lse, void* workspace, size_t ws_bytes, int32_t* err_flag,
                                    const clo_attn_opts* opts, cudaStream_t stream,
-                                   const LookupParams* lookup) {
+                                   const LookupParams* lookup, const FillParams* fill = nullptr,
+                                   int fill_ctas = 0) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Np < 0 || Np > Hkv)
         return CLO_ERR_INVALID_ARG;
     if (B == 0) return CLO_OK;  // empty batch: nothing to compute
@@ -1326,7 +1365,7 @@ static clo_status hybrid_attention(const clo_half* q, const clo_half* cbK, const
     o.Hq = Hq;
     o.G = G;
     return launch_attention(geo, o, N, HybridGeo::smem_ints(Hkv, B), B * Hkv, workspace,
-                            ws_bytes, opts, stream, lookup);
+                            ws_bytes, opts, stream, lookup, fill, fill_ctas);
 }
 
 extern "C" clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
@@ -1362,6 +1401,53 @@ extern "C" clo_status clo_hybrid_decode_attn_lookup(
     if (st != CLO_OK) return st;
     return hybrid_attention(q, cbK, cbV, idx, k, C, pK, pV, persist_ids, Np, T, B, Hq, Hkv, d,
                             scale, out, lse, workspace, ws_bytes, err_flag, opts, stream, &lk);
+}
+
+extern "C" clo_status clo_hybrid_decode_layer(
+    const clo_half* q, const clo_half* cbK, const clo_half* cbV, const int32_t* idx, int k, int C,
+    const clo_half* pK, const clo_half* pV, const int32_t* persist_ids, int Np, int T, int B,
+    int Hq, int Hkv, int d, float scale, clo_half* out, float* lse, void* workspace,
+    size_t ws_bytes, int32_t* err_flag, const clo_fill_args* fill, const clo_lookup_args* lookup,
+    const clo_attn_opts* opts, cudaStream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return CLO_ERR_INVALID_ARG;
+    if (fill != nullptr && fill->num_ctas < 0) return CLO_ERR_INVALID_ARG;
+    LookupParams lk;
+    if (lookup != nullptr) {
+        if (lookup->miss_count == nullptr || !aligned(lookup->miss_count, 4))
+            return CLO_ERR_INVALID_ARG;
+        if (B > 0) {
+            const clo_status st = make_lookup_params(
+                lookup->q, lookup->labels, lookup->w_q, lookup->tau, lookup->persist_mask, B, Hq,
+                Hkv, d, lookup->flag, lookup->sim, lookup->miss_list, lookup->miss_count, lk);
+            if (st != CLO_OK) return st;
+        }
+    }
+    FillParams fp;
+    bool no_fill = true;
+    if (fill != nullptr) {
+        const clo_status st = make_fill_params(fill->srcK, fill->srcV, fill->T, fill->tok,
+                                               fill->slot, fill->k, fill->cbK, fill->cbV, fill->C,
+                                               fill->miss_list, fill->miss_count, B, Hkv, d,
+                                               err_flag, fp, no_fill);
+        if (st != CLO_OK) return st;
+        // The fill runs beside this layer's attention and the lookup carried
+        // after it: it must not write what the attention reads, nor read the
+        // miss list the lookup writes.
+        if (!no_fill && ((cbK != nullptr && fill->cbK == cbK) || (cbV != nullptr && fill->cbV == cbV)))
+            return CLO_ERR_INVALID_ARG;
+        if (!no_fill && lookup != nullptr &&
+            (fill->miss_list == lookup->miss_list || fill->miss_count == lookup->miss_count))
+            return CLO_ERR_INVALID_ARG;
+    }
+    if (B == 0)  // nothing to attend to, fill or look up: only a lookup's miss count is written
+        return lookup == nullptr || cudaMemsetAsync(lookup->miss_count, 0, sizeof(int32_t),
+                                                    stream) == cudaSuccess
+                   ? CLO_OK
+                   : CLO_ERR_CUDA;
+    return hybrid_attention(q, cbK, cbV, idx, k, C, pK, pV, persist_ids, Np, T, B, Hq, Hkv, d,
+                            scale, out, lse, workspace, ws_bytes, err_flag, opts, stream,
+                            lookup != nullptr ? &lk : nullptr, no_fill ? nullptr : &fp,
+                            fill != nullptr ? fill->num_ctas : 0);
 }
 
 extern "C" clo_status clo_paged_decode_attn(const clo_half* q, const clo_half* kc,

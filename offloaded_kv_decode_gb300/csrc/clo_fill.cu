@@ -16,11 +16,10 @@
 // token and slot in parallel, then each half-warp moves 8 rows of K and 8 of
 // V (256 bytes each, 16 bytes a lane), all loads before any store, so every
 // lane has 16 independent 16-byte loads in flight across the host link.
-#include "clo_device.cuh"
+#include "clo_fill.cuh"
 
 namespace clo {
 
-constexpr int FILL_D = 128;  // head dimension (fp16 elements a row)
 // 4-warp CTAs, 4 an SM: the same 16 warps an SM and register cap as larger
 // CTAs, and one fill CTA fits in the room of one attention CTA, so a fill
 // launched beside an attention grid that leaves a few CTA slots free runs
@@ -30,19 +29,6 @@ constexpr int FILL_THREADS = 128;
 constexpr int FILL_WARPS = FILL_THREADS / 32;
 constexpr int FILL_ROWS = 16;  // rows a warp moves per step
 constexpr int FILL_CTAS_PER_SM = 4;
-
-struct FillParams {
-    const clo_half* srcK;
-    const clo_half* srcV;
-    const int32_t* tok;
-    const int32_t* slot;  // nullptr: slot = token
-    clo_half* cbK;
-    clo_half* cbV;
-    const int32_t* miss_list;
-    const int32_t* miss_count;
-    int32_t* err_flag;
-    int T, k, C, n_heads;  // n_heads = B * Hkv
-};
 
 // A 16-byte load that does not allocate in L1 (the source is read once).
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -66,9 +52,8 @@ __device__ __forceinline__ void st_row(void* p, const uint4& v, uint64_t policy)
                  : "memory");
 }
 
-__global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM) fill_kernel(const FillParams p) {
-    pdl_launch_dependents();
-    pdl_wait();  // the miss list comes from the kernel before
+// The rows of the miss list, moved by the grid's warps.
+__device__ __forceinline__ void fill_rows(const FillParams& p) {
     int count = *p.miss_count;
     if (count < 0 || count > p.n_heads) {
         if (blockIdx.x == 0 && threadIdx.x == 0) report_error(p.err_flag, CLO_FLAG_BAD_INDEX);
@@ -127,6 +112,23 @@ __global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM) fill_kernel(co
     if (bad) report_error(p.err_flag, CLO_FLAG_BAD_INDEX);
 }
 
+__global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM) fill_kernel(const FillParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the miss list comes from the kernel before
+    fill_rows(p);
+}
+
+// The fill launched beside the kernel before it (see launch_fill): the miss
+// list was written before that kernel started, so the rows move at once, and
+// the wait at the end keeps this grid from finishing before that kernel, so
+// the kernels after it see both finished.
+__global__ void __launch_bounds__(FILL_THREADS, FILL_CTAS_PER_SM)
+    fill_beside_kernel(const FillParams p) {
+    pdl_launch_dependents();
+    fill_rows(p);
+    pdl_wait();
+}
+
 // Resolves the address the device reads a source buffer through.  Device and
 // managed memory are used as they are; pinned host memory through its mapped
 // device address; other host memory only where the device can read pageable
@@ -151,16 +153,11 @@ static bool device_readable(const void*& p) {
     return pageable != 0;
 }
 
-}  // namespace clo
-
-using namespace clo;
-
-extern "C" clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int T,
-                                            const int32_t* tok, const int32_t* slot, int k,
-                                            clo_half* cbK, clo_half* cbV, int C,
-                                            const int32_t* miss_list, const int32_t* miss_count,
-                                            int B, int Hkv, int d, int32_t* err_flag,
-                                            const clo_attn_opts* opts, cudaStream_t stream) {
+clo_status make_fill_params(const clo_half* srcK, const clo_half* srcV, int T, const int32_t* tok,
+                            const int32_t* slot, int k, clo_half* cbK, clo_half* cbV, int C,
+                            const int32_t* miss_list, const int32_t* miss_count, int B, int Hkv,
+                            int d, int32_t* err_flag, FillParams& p, bool& nothing) {
+    nothing = false;
     if (B < 0 || Hkv <= 0 || T < 0 || k < 0 || C < 0) return CLO_ERR_INVALID_ARG;
     if (d != FILL_D) return CLO_ERR_UNSUPPORTED;
     if (miss_count == nullptr) return CLO_ERR_INVALID_ARG;
@@ -168,7 +165,10 @@ extern "C" clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half
     if (n_heads > (1ll << 30) || static_cast<long long>(T) * n_heads > (1ll << 40) ||
         static_cast<long long>(C) * n_heads > (1ll << 40))
         return CLO_ERR_UNSUPPORTED;
-    if (B == 0 || k == 0) return CLO_OK;  // nothing to move
+    if (B == 0 || k == 0) {  // nothing to move
+        nothing = true;
+        return CLO_OK;
+    }
     if (srcK == nullptr || srcV == nullptr || tok == nullptr || cbK == nullptr ||
         cbV == nullptr || miss_list == nullptr)
         return CLO_ERR_INVALID_ARG;
@@ -184,7 +184,6 @@ extern "C" clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half
     const void* rV = srcV;
     if (!device_readable(rK) || !device_readable(rV)) return CLO_ERR_INVALID_ARG;
 
-    FillParams p;
     p.srcK = static_cast<const clo_half*>(rK);
     p.srcV = static_cast<const clo_half*>(rV);
     p.tok = tok;
@@ -198,19 +197,44 @@ extern "C" clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half
     p.k = k;
     p.C = C;
     p.n_heads = static_cast<int>(n_heads);
-    // One wave, no more warps than 16-row steps of the largest possible list.
+    return CLO_OK;
+}
+
+long long fill_max_grid(const FillParams& p) {
     const int sms = device_sm_count();
-    if (sms <= 0) return CLO_ERR_CUDA;
-    const long long max_steps = (n_heads * k + FILL_ROWS - 1) / FILL_ROWS;
+    if (sms <= 0) return 0;
+    const long long max_steps = (static_cast<long long>(p.n_heads) * p.k + FILL_ROWS - 1) / FILL_ROWS;
     long long grid = (max_steps + FILL_WARPS - 1) / FILL_WARPS;
     if (grid > static_cast<long long>(sms) * FILL_CTAS_PER_SM) grid = static_cast<long long>(sms) * FILL_CTAS_PER_SM;
+    return grid < 1 ? 1 : grid;
+}
+
+cudaError_t launch_fill(const FillParams& p, int grid, bool beside, cudaStream_t stream) {
+    return launch_pdl(beside ? fill_beside_kernel : fill_kernel, dim3(static_cast<unsigned>(grid)),
+                      dim3(FILL_THREADS), 0, stream, p);
+}
+
+}  // namespace clo
+
+using namespace clo;
+
+extern "C" clo_status clo_fill_cache_buffer(const clo_half* srcK, const clo_half* srcV, int T,
+                                            const int32_t* tok, const int32_t* slot, int k,
+                                            clo_half* cbK, clo_half* cbV, int C,
+                                            const int32_t* miss_list, const int32_t* miss_count,
+                                            int B, int Hkv, int d, int32_t* err_flag,
+                                            const clo_attn_opts* opts, cudaStream_t stream) {
+    FillParams p;
+    bool nothing = false;
+    const clo_status st = make_fill_params(srcK, srcV, T, tok, slot, k, cbK, cbV, C, miss_list,
+                                           miss_count, B, Hkv, d, err_flag, p, nothing);
+    if (st != CLO_OK || nothing) return st;
+    long long grid = fill_max_grid(p);
+    if (grid <= 0) return CLO_ERR_CUDA;
     if (opts != nullptr && opts->num_ctas > 0) grid = opts->num_ctas;
-    if (grid < 1) grid = 1;
     if (opts != nullptr && opts->ev_begin != nullptr && !record_event(opts->ev_begin, stream))
         return CLO_ERR_CUDA;
-    if (launch_pdl(fill_kernel, dim3(static_cast<unsigned>(grid)), dim3(FILL_THREADS), 0, stream, p) !=
-        cudaSuccess)
-        return CLO_ERR_CUDA;
+    if (launch_fill(p, static_cast<int>(grid), false, stream) != cudaSuccess) return CLO_ERR_CUDA;
     if (opts != nullptr && opts->ev_end != nullptr && !record_event(opts->ev_end, stream))
         return CLO_ERR_CUDA;
     return CLO_OK;

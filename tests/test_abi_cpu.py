@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert len(names) == 20, names
+    assert len(names) == 21, names
     for n in names:
         assert hasattr(L, n), f"{n} declared in clo.h but not exported"
 
@@ -196,6 +196,41 @@ def test_fused_lookup_rejects(L):
     assert fused(B=9000) == clo.CLO_ERR_UNSUPPORTED
 
 
+def test_layer_rejects(L):
+    """clo_hybrid_decode_layer checks its carried fill and lookup before
+    anything launches (none of these cases reaches the device)."""
+    def layer(B=1, Hq=32, Hkv=8, fill=None, lookup=None):
+        return L.clo_hybrid_decode_layer(
+            FAKE, FAKE, FAKE, FAKE, 10, 100, FAKE, FAKE, FAKE, 2, 50, B, Hq, Hkv, 128, 0.088,
+            FAKE, None, FAKE, 1 << 30, None,
+            None if fill is None else ctypes.byref(fill),
+            None if lookup is None else ctypes.byref(lookup), None, None)
+
+    def fill(**kw):
+        a = dict(srcK=FAKE, srcV=FAKE, T=64, tok=FAKE, slot=FAKE, k=8, cbK=FAKE + 4096,
+                 cbV=FAKE + 8192, C=64, miss_list=FAKE, miss_count=FAKE, num_ctas=0)
+        a.update(kw)
+        return clo.FillArgs(**a)
+
+    def lookup(**kw):
+        a = dict(q=FAKE, labels=FAKE, w_q=FAKE, tau=FAKE, persist_mask=None, flag=FAKE,
+                 sim=FAKE, miss_list=FAKE + 256, miss_count=FAKE + 256)
+        a.update(kw)
+        return clo.LookupArgs(**a)
+
+    assert layer(B=-1) == clo.CLO_ERR_INVALID_ARG
+    assert layer(Hq=30) == clo.CLO_ERR_INVALID_ARG
+    assert layer(fill=fill(num_ctas=-1)) == clo.CLO_ERR_INVALID_ARG
+    assert layer(fill=fill(tok=None)) == clo.CLO_ERR_INVALID_ARG
+    assert layer(fill=fill(miss_count=None)) == clo.CLO_ERR_INVALID_ARG
+    assert layer(fill=fill(slot=None, C=32)) == clo.CLO_ERR_INVALID_ARG  # token rows need C >= T
+    assert layer(fill=fill(srcK=FAKE + 2)) == clo.CLO_ERR_INVALID_ARG   # misaligned rows
+    assert layer(lookup=lookup(q=None)) == clo.CLO_ERR_INVALID_ARG
+    assert layer(lookup=lookup(miss_count=None)) == clo.CLO_ERR_INVALID_ARG
+    assert layer(lookup=lookup(q=FAKE + 2)) == clo.CLO_ERR_INVALID_ARG
+    assert layer(B=0, fill=fill()) == clo.CLO_OK  # empty batch, no lookup: nothing to do
+
+
 def test_topk_rejects(L):
     def topk(q=FAKE, K=FAKE, B=1, Hq=32, Hkv=8, T=100, d=128, k=10, ws=FAKE, wsb=1 << 30):
         return L.clo_topk_retrieve(q, K, B, Hq, Hkv, T, d, k, FAKE, ws, wsb, None, None)
@@ -242,6 +277,13 @@ def test_header_is_plain_c_and_links(L, tmp_path):
         "    uint32_t ready = 0;\n"
         "    if (clo_signal_ready(&ready, 42u) != CLO_OK || ready != 42u) return 9;\n"
         "    if (clo_wait_ready(&ready, 42u, 0u, NULL, 0) != CLO_ERR_INVALID_ARG) return 10;\n"
+        "    /* the layer call's carried fill, declared in C */\n"
+        "    clo_fill_args f;\n"
+        "    memset(&f, 0, sizeof f);\n"
+        "    f.k = 8; f.T = 64; f.C = 64;\n"
+        "    if (clo_hybrid_decode_layer(NULL, NULL, NULL, NULL, 10, 100, NULL, NULL, NULL, 2, 50,\n"
+        "                                1, 32, 8, 128, 0.088f, NULL, NULL, NULL, 0, NULL, &f, NULL,\n"
+        "                                NULL, 0) != CLO_ERR_INVALID_ARG) return 11;\n"
         '    printf("%d %d %d %d %d\\n", np_, npers[0], ids[0], ids[1], ids[2]);\n'
         "    return 0;\n}\n")
     exe = tmp_path / "use_clo"

@@ -16,6 +16,7 @@ pytestmark = pytest.mark.gpu
     ["--workload", "tiny"],
     ["--workload", "tiny", "--lookup-schedule", "stream"],
     ["--workload", "tiny", "--lookup-schedule", "serial"],
+    ["--workload", "tiny", "--lookup-schedule", "pipelined"],
     ["--workload", "paged_llama2_7b_b256", "--batch", "8"],
     ["--workload", "fill_hbm_llama3_8b_b8_32k", "--batch", "1"],
     ["--workload", "fill_c2c_llama3_8b_b8_32k", "--batch", "1"],
@@ -28,6 +29,8 @@ pytestmark = pytest.mark.gpu
      "overlap"],
     ["--workload", "llama3_8b_layer_b8_32k_miss_fill", "--batch", "1", "--lookup-schedule",
      "stream"],
+    ["--workload", "llama3_8b_layer_b8_32k_miss_fill", "--batch", "1", "--lookup-schedule",
+     "pipelined"],
 ], ids=lambda a: "_".join(x.lstrip("-") for x in a[1::2] if x not in ("--batch",)))
 def test_bench_line(args):
     buf = io.StringIO()
@@ -54,17 +57,18 @@ def test_bench_line(args):
 def test_overlapped_fill_schedule_orders_the_fill_before_its_attention():
     """The miss-path fill on the second stream (the next layer's fill beside
     the current layer's attention, "overlap"; or lookup and fill there,
-    "stream") must leave every layer's attention output bit-identical to the
-    serial schedule's with the same CTA counts: an attention that ran before
-    its fill would read the old rows (the full KV copy holds other values
-    than the Cache Buffer)."""
+    "stream"), or carried beside the attention in one layer call
+    ("pipelined"), must leave every layer's attention output bit-identical to
+    the serial schedule's with the same CTA counts: an attention that ran
+    before its fill would read the old rows (the full KV copy holds other
+    values than the Cache Buffer)."""
     import torch
     import workloads as wl
 
     cfg = dataclasses.replace(wl.CONFIGS["llama3_8b_layer_b8_32k_miss_fill"], B=1)
     dev = torch.device("cuda:0")
     outs = {}
-    for sched in ("serial", "overlap", "stream"):
+    for sched in ("serial", "overlap", "stream", "pipelined"):
         W = bench.HybridWorkload(cfg, dev, 0, replicas=3, schedule=sched, side_ctas=32)
         assert W.misses_per_step > 0
         for i in range(2 * W.n_inst):  # every buffer set filled at least once
@@ -79,7 +83,7 @@ def test_overlapped_fill_schedule_orders_the_fill_before_its_attention():
         outs[sched] = [it["out"].clone() for it in W.inst]
         del W
         torch.cuda.empty_cache()
-    for sched in ("overlap", "stream"):
+    for sched in ("overlap", "stream", "pipelined"):
         for a, b in zip(outs["serial"], outs[sched]):
             assert not torch.isnan(a).any()
             assert torch.equal(a, b), sched
@@ -89,7 +93,8 @@ def test_overlapped_fill_schedule_across_layers():
     """The same check on a three-layer step with a ring of five buffer sets
     and the fill from a full KV copy in HBM: the attention of layer l+1 must
     wait for the fill issued beside layer l, for every l, and for the next
-    step's layer 0."""
+    step's layer 0 (with "pipelined" the lookups run two layers ahead, so the
+    step's last two calls look up the next step's first two layers)."""
     import torch
     import workloads as wl
 
@@ -98,7 +103,7 @@ def test_overlapped_fill_schedule_across_layers():
                           miss_fill="device", ring=5, seed=4242)
     dev = torch.device("cuda:0")
     outs = {}
-    for sched in ("serial", "overlap"):
+    for sched in ("serial", "overlap", "pipelined"):
         W = bench.HybridWorkload(cfg, dev, 0, schedule=sched, side_ctas=24)
         assert W.n_inst == 5 and W.misses_per_step > 0
         for i in range(4 * W.n_inst):
@@ -113,6 +118,7 @@ def test_overlapped_fill_schedule_across_layers():
         outs[sched] = [it["out"].clone() for it in W.inst]
         del W
         torch.cuda.empty_cache()
-    for a, b in zip(outs["serial"], outs["overlap"]):
-        assert not torch.isnan(a).any()
-        assert torch.equal(a, b)
+    for sched in ("overlap", "pipelined"):
+        for a, b in zip(outs["serial"], outs[sched]):
+            assert not torch.isnan(a).any()
+            assert torch.equal(a, b), sched
