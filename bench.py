@@ -199,16 +199,17 @@ class HybridWorkload:
                    max(1, n_tiles // 8))
         self.attn_kernels = 2 if ctas >= 2 else 1
         self.phases = self.n_inst // math.gcd(self.L, self.n_inst)
-        # "overlap": the next layer's fill runs on a second stream beside this
-        # layer's attention.  The fill takes side_ctas CTAs (each fits in the
-        # room of one attention CTA) and the attention grid leaves that many of
-        # its 3 x SMs slots free, so both are resident at once.  (None: 64 with
-        # that schedule, else the full grids; a number applies to any schedule.)
-        if side_ctas is None:
-            side_ctas = 64 if schedule == "overlap" or (schedule == "pipelined" and
-                                                          cfg.miss_fill) else 0
-        self.side_ctas = side_ctas
+        # "overlap" and "pipelined": the next layer's fill runs beside this
+        # layer's attention (on a second stream, or in the same layer call).
+        # The fill takes side_ctas CTAs (each fits in the room of one attention
+        # CTA) and the attention grid leaves that many of its 3 x SMs slots
+        # free, so both are resident at once.  (None: the measured best of
+        # each schedule, else the full grids; a number applies to any schedule.)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        if side_ctas is None:  # for the layer call, the library's default share (a quarter)
+            side_ctas = 64 if schedule == "overlap" else \
+                (3 * sms) // 4 if (schedule == "pipelined" and cfg.miss_fill) else 0
+        self.side_ctas = side_ctas
         self.main_ctas = max(1, 3 * sms - self.side_ctas) if self.side_ctas else 0
         self.fill_ctas = self.side_ctas
         self.lab0_all = self.lab_all.clone()

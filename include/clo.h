@@ -357,7 +357,7 @@ typedef struct clo_fill_args {
     int C;
     const int32_t* miss_list;
     const int32_t* miss_count;
-    int num_ctas; /* CTAs of the fill; 0 = one in seven of the default attention grid's slots,
+    int num_ctas; /* CTAs of the fill; 0 = a quarter of the default attention grid's slots,
                      at most as many as the longest possible miss list keeps busy */
 } clo_fill_args;
 

@@ -92,11 +92,6 @@ constexpr int MAX_ROWS = 1 << 24;  // rows per head: row offsets stay 32-bit
 constexpr int SMEM_LIMIT = 227 * 1024;     // per CTA
 constexpr int SMEM_PER_SM = 228 * 1024;    // per SM, 1 KB of it reserved per resident CTA
 constexpr int MERGE_SMEM_LIMIT = 96 * 1024;
-// Default share of the main kernel's CTA slots given to a fill carried beside
-// it: one in FILL_SHARE (65 of 456 on 152 SMs).  On the B8 32K layer and the
-// B1 128K step, with misses fetched over the host link, 48 to 96 fill CTAs
-// were within 2% of the best step time.
-constexpr int FILL_SHARE = 7;
 
 // One token set: batch row (or request) b, KV head kv.
 struct Seg {
@@ -1225,13 +1220,10 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
     const int wave = device_sm_count() * per_sm;
     if (wave <= 0) return CLO_ERR_CUDA;
     // A fill carried beside the main kernel runs in CTA slots the main grid
-    // leaves free (a fill CTA fits in the room of one main-kernel CTA): by
-    // default one slot in FILL_SHARE, never more CTAs than the largest fill
-    // can use.
+    // leaves free (a fill CTA fits in the room of one main-kernel CTA).
     long long fill_grid = 0;
     if (fill != nullptr) {
-        fill_grid = fill_ctas > 0 ? fill_ctas
-                                  : std::min(std::max(wave / FILL_SHARE, 1), static_cast<int>(fill_max_grid(*fill)));
+        fill_grid = fill_ctas > 0 ? fill_ctas : fill_beside_default_ctas(*fill, wave);
         if (fill_grid <= 0) return CLO_ERR_CUDA;
     }
     int C = (opts != nullptr && opts->num_ctas > 0)

@@ -209,6 +209,20 @@ long long fill_max_grid(const FillParams& p) {
     return grid < 1 ? 1 : grid;
 }
 
+// A quarter of the wave (114 of 456 CTA slots on 152 SMs).  Layer calls with
+// misses fetched over the host link, µs per layer-step on one box: the B8 32K
+// layer 95.2 / 93.8 / 93.5 / 96.1 and the B1 128K step 58.5 / 57.1 / 56.1 /
+// 56.0 with 64 / 96 / 128 / 160 fill CTAs.  Fewer CTAs keep too little in
+// flight on the link; more take too many slots from the attention.
+constexpr int FILL_BESIDE_SHARE = 4;
+
+long long fill_beside_default_ctas(const FillParams& p, int wave) {
+    long long n = wave / FILL_BESIDE_SHARE;
+    const long long most = fill_max_grid(p);
+    if (n > most) n = most;
+    return n < 1 ? 1 : n;
+}
+
 cudaError_t launch_fill(const FillParams& p, int grid, bool beside, cudaStream_t stream) {
     return launch_pdl(beside ? fill_beside_kernel : fill_kernel, dim3(static_cast<unsigned>(grid)),
                       dim3(FILL_THREADS), 0, stream, p);

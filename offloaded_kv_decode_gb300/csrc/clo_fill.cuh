@@ -36,6 +36,11 @@ clo_status make_fill_params(const clo_half* srcK, const clo_half* srcV, int T, c
 // warps than 16-row steps of the longest possible miss list.
 long long fill_max_grid(const FillParams& p);
 
+// CTAs of a fill carried beside a kernel whose full grid is `wave` CTAs (that
+// kernel then runs with this many fewer): a share of the wave, at least 1, at
+// most fill_max_grid(p).
+long long fill_beside_default_ctas(const FillParams& p, int wave);
+
 // Launches the fill with `grid` CTAs on `stream`.
 //  beside = false: the fill waits for the kernel before it (the lookup that
 //    wrote the miss list) before it reads anything.
