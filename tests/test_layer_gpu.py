@@ -165,22 +165,25 @@ def _fill_tuple(x, s):
     return (x["srcK"], x["srcV"], x["idx"], None, s["cbK"], s["cbV"], s["miss"], s["count"])
 
 
-@pytest.mark.parametrize("host_src", [True, False], ids=["host_src", "hbm_src"])
-def test_layer_chain_equals_serial(host_src):
+@pytest.mark.parametrize("host_src,full_wave", [(True, False), (False, False), (True, True)],
+                         ids=["host_src", "hbm_src", "host_src_full_wave"])
+def test_layer_chain_equals_serial(host_src, full_wave):
     """Five layers.  Serial: per layer lookup, fill, attention, one after
     another.  Pipelined: lookups of layers 0 and 1 and the fill of layer 0
     first, then one clo_hybrid_decode_layer call per layer (attention l, fill
     l+1 beside it, lookup l+2 in its merge launch).  Every output, label,
     lookup result and Cache Buffer must be bit-identical; the attentions use
-    the same grid in both."""
+    the same grid in both.  With full_wave the attention takes every CTA slot,
+    so the fill's CTAs find room only as attention CTAs finish (nothing the
+    attention does waits for the fill, so the call still completes)."""
     cfg = wl.small_hybrid("chain", B=4, Hq=32, Hkv=8, T=4096, Np=2, qmode="cos", c_lo=0.5,
                           c_hi=0.95, seed=5300)
     d = dev()
     L = 5
     layers = _chain_layers(cfg, L, d, host_src)
     sms = torch.cuda.get_device_properties(d).multi_processor_count
-    fill_ctas = 48
-    main_ctas = 3 * sms - fill_ctas
+    fill_ctas = 64 if full_wave else 48
+    main_ctas = 3 * sms if full_wave else 3 * sms - fill_ctas
     ws = torch.empty(clo.clo_hybrid_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, 128, main_ctas),
                      dtype=torch.uint8, device=d)
     err = torch.zeros(1, dtype=torch.int32, device=d)
