@@ -256,3 +256,92 @@ def test_fused_lookup_random_shape(i):
     got = dict(flag=flag.cpu().numpy(), sim=sim.cpu().numpy(), labels=labd.cpu().numpy(),
                miss_list=miss.cpu().numpy()[:max(m, 0)], miss_count=m)
     assert_lookup_matches(ref_lk, got, tau, pm, G)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_layer_call_random_shape(i):
+    """clo_hybrid_decode_layer on a random shape: the attention against the
+    oracle's, the next layer's fill (a random miss list, rows from pinned host
+    memory or HBM, token or compact addressing) bit for bit, and the carried
+    lookup (about half the KV heads at s = 1) against oracle_lookup_update."""
+    from gpu_util import assert_lookup_matches
+
+    B, Hq, Hkv, T, k, Np, C, num_ctas = _hybrid_shape(700 + i)
+    G = Hq // Hkv
+    r = np.random.Generator(np.random.PCG64(4000 + i))
+    f16 = lambda *s: r.standard_normal(s).astype(np.float16)
+    q = f16(B, Hq, 128)
+    cbK, cbV = f16(B, Hkv, C, 128), f16(B, Hkv, C, 128)
+    idx = np.stack([np.stack([r.permutation(C)[:k] for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    pK, pV = f16(B, Np, T, 128), f16(B, Np, T, 128)
+    pid = r.permutation(Hkv)[:Np].astype(np.int32)
+    # The fill: the next layer's full KV copy, its new top-k tokens and their rows.
+    Tf = int(r.integers(1, 2000))
+    kf = int(r.integers(1, Tf + 1))
+    compact = bool(r.integers(0, 2))
+    Cf = kf if compact else Tf
+    srcK, srcV = f16(B, Hkv, Tf, 128), f16(B, Hkv, Tf, 128)
+    tok = np.stack([np.stack([r.permutation(Tf)[:kf] for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    slot = np.stack([np.stack([r.permutation(kf) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32) if compact else None
+    fK0, fV0 = f16(B, Hkv, Cf, 128), f16(B, Hkv, Cf, 128)
+    fmiss = sorted(r.permutation(B * Hkv)[:int(r.integers(0, B * Hkv + 1))].tolist())
+    host_src = bool(r.integers(0, 2))
+    fill_ctas = int(r.choice([0, 0, 1, 7, 40]))
+    # The lookup of the layer after.
+    lab = r.standard_normal((B, Hq, 128))
+    qn = (0.8 * lab + 0.6 * r.standard_normal((B, Hq, 128))).astype(np.float16)
+    lab = lab.astype(np.float16)
+    s = r.uniform(0, 1, Hq).astype(np.float32)
+    for g in range(Hkv):
+        if r.integers(0, 2):
+            s[g * G:(g + 1) * G] = 1.0
+    tau = clo.clo_thresholds_host(s, Hkv, G)
+    pm = np.zeros(Hkv, dtype=np.uint8)
+    pm[r.permutation(Hkv)[:int(r.integers(0, Hkv + 1))]] = 1
+    orc = oracle.get()
+    ref, ref_lse = orc.hybrid_attn(q, cbK, cbV, idx, pK, pV, pid, scale_for())
+    rK, rV, rc = orc.fill_cache_buffer(srcK, srcV, tok, slot, fK0, fV0, fmiss)
+    assert rc == 0
+    ref_lk = orc.lookup_update(qn, lab, s.astype(np.float64), tau.astype(np.float64), pm)
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    h = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    d = dev()
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device=d)
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=d)
+    ws = torch.empty(clo.clo_hybrid_workspace_size(B, Hq, Hkv, 128, num_ctas), dtype=torch.uint8,
+                     device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    fK, fV = t(fK0), t(fV0)
+    fml = torch.full((B * Hkv,), -3, dtype=torch.int32)
+    fml[:len(fmiss)] = torch.tensor(fmiss, dtype=torch.int32)
+    fill = ((h(srcK), h(srcV)) if host_src else (t(srcK), t(srcV))) + \
+        (t(tok), None if slot is None else t(slot), fK, fV, fml.to(d),
+         torch.tensor([len(fmiss)], dtype=torch.int32, device=d))
+    labd = t(lab)
+    n = B * Hkv
+    flag = torch.full((n,), 9, dtype=torch.uint8, device=d)
+    sim = torch.full((n,), -9.0, device=d)
+    miss = torch.full((n,), -9, dtype=torch.int32, device=d)
+    cnt = torch.full((1,), -9, dtype=torch.int32, device=d)
+    has_cb = Np < Hkv
+    clo.clo_hybrid_decode_layer(
+        t(q), t(cbK) if has_cb else None, t(cbV) if has_cb else None, t(idx) if has_cb else None,
+        t(pK) if Np else None, t(pV) if Np else None, t(pid) if Np else None, out, ws,
+        fill=fill, lookup=(t(qn), labd, t(s), t(tau), t(pm), flag, sim, miss, cnt), lse=lse,
+        err_flag=err, num_ctas=num_ctas, fill_ctas=fill_ctas)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    what = (f"case {i}: B{B} Hq{Hq} Hkv{Hkv} T{T} k{k} Np{Np} C{C} ctas{num_ctas}; fill T{Tf} "
+            f"k{kf} C{Cf} {len(fmiss)} heads {'host' if host_src else 'hbm'} ctas{fill_ctas}")
+    assert_close(out.cpu().numpy(), ref, what)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) < LSE_ATOL, what
+    assert np.array_equal(fK.cpu().numpy().view(np.uint16), rK), what
+    assert np.array_equal(fV.cpu().numpy().view(np.uint16), rV), what
+    m = int(cnt.item())
+    got = dict(flag=flag.cpu().numpy(), sim=sim.cpu().numpy(), labels=labd.cpu().numpy(),
+               miss_list=miss.cpu().numpy()[:max(m, 0)], miss_count=m)
+    assert_lookup_matches(ref_lk, got, tau, pm, G)
