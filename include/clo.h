@@ -16,9 +16,10 @@
  * Around them: the miss-path fill that writes missed heads' top-k rows into
  * the Cache Buffer (CLO section 3, Fig. 7), the offline persistent-head plan
  * (CLO Eqs. 11-13), the next layer's lookup carried in an attention launch
- * (CLO section 3, Fig. 9), top-k retrieval by exact qk-score (CLO Eq. 6) and
- * the GPU-centric data-ready synchronisation with a bounded wait (CLO
- * section 2, Fig. 8).
+ * and one layer of the decode flow in one call, with the next layer's fill
+ * beside the attention (CLO section 3, Fig. 9), top-k retrieval by exact
+ * qk-score (CLO Eq. 6) and the GPU-centric data-ready synchronisation with a
+ * bounded wait (CLO section 2, Fig. 8).
  *
  * Conventions shared by every entry point:
  *  - Tensor pointers are DEVICE pointers owned by the caller (unless a call
