@@ -1377,6 +1377,27 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+def shape_config(name: str) -> dict:
+    """The workload's name and shape, from its configuration alone (no device
+    memory): the keys the reference arm reports, as the GPU arm's `config`
+    reports them."""
+    if name in wl.CONFIGS:
+        c = wl.CONFIGS[name]
+        return {"workload": c.name, "batch": c.B, "layers": c.L, "q_heads": c.Hq,
+                "kv_heads": c.Hkv, "head_dim": c.d, "context": c.T, "top_k": c.k,
+                "persistent_heads": c.Np, "cache_buffer": c.addressing}
+    if name in wl.PAGED_CONFIGS:
+        c = wl.PAGED_CONFIGS[name]
+        return {"workload": c.name, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv,
+                "head_dim": c.d, "context": f"U[{c.ctx_lo},{c.ctx_hi}]",
+                "block_size": c.block_size,
+                "tokens": int(wl.paged_context_lengths(c).sum())}
+    base = wl.FILL_CONFIGS[name][0] if name in wl.FILL_CONFIGS else wl.TOPK_CONFIGS[name]
+    c = wl.CONFIGS[base]
+    return {"workload": name, "base": base, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv,
+            "head_dim": c.d, "context": c.T, "top_k": c.k}
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -1408,7 +1429,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes of the pages' workloads)",
-        "config": {"workload": args.workload},
+        "config": shape_config(args.workload),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {desc}, run for {per_step:.1f} s on {cores} host "
                                    f"thread(s)"},

@@ -54,3 +54,19 @@ def test_reference_arm_only_rank0_prints(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"])
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line(capsys, monkeypatch):
+    """Rank 0 prints the reference arm's line: the oracle on the host cores,
+    on the same workload shape as the GPU arm's config."""
+    import json
+
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"])
+    d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["config"] == bench.shape_config("tiny")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
