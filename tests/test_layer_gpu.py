@@ -335,3 +335,57 @@ def test_layer_empty_batch_and_empty_fill():
                                 None, None, None, q.clone(), ws, lookup=lk)
     torch.cuda.synchronize()
     assert int(cnt.item()) == 0
+
+
+def test_layer_calls_captured_in_a_graph():
+    """Three chained layer calls captured into a CUDA graph and replayed give
+    exactly what the same calls give issued one by one: the fill beside each
+    attention and the programmatic-launch edges survive capture."""
+    cfg = wl.small_hybrid("graph_chain", B=2, Hq=32, Hkv=8, T=2048, Np=2, qmode="cos", c_lo=0.5,
+                          c_hi=0.95, seed=5400)
+    d = dev()
+    L = 4
+    layers = _chain_layers(cfg, L, d, True)
+    ws = torch.empty(clo.clo_hybrid_workspace_size(cfg.B, cfg.Hq, cfg.Hkv), dtype=torch.uint8,
+                     device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+
+    def prologue(st):
+        clo.clo_lookup_update(*_lookup_tuple(layers[0], st[0]))
+        clo.clo_lookup_update(*_lookup_tuple(layers[1], st[1]))
+        clo.clo_fill_cache_buffer(*_fill_tuple(layers[0], st[0]), err_flag=err)
+
+    def calls(st):
+        for l in range(L - 1):
+            x = layers[l]
+            fill = _fill_tuple(layers[l + 1], st[l + 1])
+            look = _lookup_tuple(layers[l + 2], st[l + 2]) if l + 2 < L else None
+            clo.clo_hybrid_decode_layer(x["q"], st[l]["cbK"], st[l]["cbV"], x["idx"], x["pK"],
+                                        x["pV"], x["pid"], st[l]["out"], ws, fill=fill,
+                                        lookup=look, err_flag=err)
+
+    eager = _fresh(cfg, layers, d)
+    prologue(eager)
+    calls(eager)
+    torch.cuda.synchronize()
+    graph = _fresh(cfg, layers, d)
+    prologue(graph)
+    torch.cuda.synchronize()
+    # Warm the calls once on a side stream (kernel attributes are set outside capture).
+    warm = _fresh(cfg, layers, d)
+    prologue(warm)
+    calls(warm)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            calls(graph)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for l in range(L):
+        for key in ("out", "cbK", "cbV", "lab", "flag", "sim"):
+            if key == "out" and l == L - 1:
+                continue  # the last layer's attention is not in the captured calls
+            assert torch.equal(eager[l][key], graph[l][key]), f"layer {l}: {key}"
