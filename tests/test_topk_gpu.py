@@ -123,3 +123,74 @@ def test_topk_full_size_every_head():
     swaps = [one((b, h)) for b in range(B) for h in range(Hkv)]
     assert sum(swaps) <= B * Hkv
     print(f"top-k full size: 64 heads, {sum(swaps)} boundary swaps")
+
+
+def test_retrieval_fill_attention_chain():
+    """CLO's miss path with retrieval, on one stream with no host round trip:
+    the lookup flags the missed heads; top-k retrieval ranks every key of
+    every head against the queries (CLO Eq. 6); the fill copies the missed
+    heads' new top-k rows from the full KV copy in pinned host memory into
+    the token-addressed Cache Buffer; the attention reads them through the
+    same indices.  The retrieval is checked against the oracle's as above,
+    and the oracle then runs the lookup, fill and attention on the indices the
+    GPU chose, which the GPU results must match (the fill bit for bit)."""
+    import workloads as wl
+    from gpu_util import assert_close, scale_for
+
+    cfg = wl.small_hybrid("retrieval_chain", B=2, Hq=32, Hkv=8, T=1200, Np=2, qmode="cos",
+                          c_lo=0.5, c_hi=0.95, seed=5500)
+    orc = oracle.get()
+    d = dev()
+    q, lab = wl.queries_and_labels(cfg, 0, "cpu")
+    srcK, srcV = wl.full_kv(cfg, 0, "cpu")
+    cbK, cbV, _ = wl.cache_buffer(cfg, 0, "cpu")  # old rows, partly overwritten by the fill
+    pK, pV = wl.persistent_cache(cfg, 0, "cpu")
+    pid = wl.persist_ids(cfg, 0)
+    pm = wl.persist_mask(cfg, 0)
+    s = np.ones(cfg.Hq, dtype=np.float32)  # tau = eta: groups with cosine below 0.8 miss
+    tau = clo.clo_thresholds_host(s, cfg.Hkv, cfg.G, 0.8, 3.0)
+
+    qd, labd = q.to(d), lab.to(d)
+    n = cfg.B * cfg.Hkv
+    flag = torch.empty(n, dtype=torch.uint8, device=d)
+    sim = torch.empty(n, dtype=torch.float32, device=d)
+    ml = torch.empty(n, dtype=torch.int32, device=d)
+    mc = torch.empty(1, dtype=torch.int32, device=d)
+    idx = torch.empty((cfg.B, cfg.Hkv, cfg.k), dtype=torch.int32, device=d)
+    tws = torch.empty(clo.clo_topk_workspace_size(cfg.B, cfg.Hkv, cfg.T), dtype=torch.uint8,
+                      device=d)
+    gK, gV = cbK.to(d), cbV.to(d)
+    out = torch.empty_like(qd)
+    ws = torch.empty(clo.clo_hybrid_workspace_size(cfg.B, cfg.Hq, cfg.Hkv), dtype=torch.uint8,
+                     device=d)
+    err = torch.zeros(1, dtype=torch.int32, device=d)
+    hK, hV = srcK.pin_memory(), srcV.pin_memory()
+    clo.clo_lookup_update(qd, labd, torch.from_numpy(s).to(d), torch.from_numpy(tau).to(d),
+                          torch.from_numpy(pm).to(d), flag, sim, ml, mc)
+    clo.clo_topk_retrieve(qd, srcK.to(d), cfg.k, idx, tws)
+    clo.clo_fill_cache_buffer(hK, hV, idx, None, gK, gV, ml, mc, err_flag=err)
+    clo.clo_hybrid_decode_attn(qd, gK, gV, idx, pK.to(d), pV.to(d), torch.from_numpy(pid).to(d),
+                               out, ws, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+    # The retrieval against the oracle's (boundary swaps inside the fp32 band only).
+    got_idx = idx.cpu().numpy()
+    ref_idx = orc.topk_retrieve(q.numpy(), srcK.numpy(), cfg.k)
+    q64, K64 = q.numpy().astype(np.float64), srcK.numpy().astype(np.float64)
+    for b in range(cfg.B):
+        for g in range(cfg.Hkv):
+            check_head(got_idx[b, g], ref_idx[b, g], q64[b, g * cfg.G:(g + 1) * cfg.G].sum(0),
+                       K64[b, g], cfg.k)
+    # The oracle chain on the GPU's indices.
+    lk = orc.lookup_update(q.numpy(), lab.numpy(), s.astype(np.float64), tau.astype(np.float64),
+                           pm)
+    assert not (np.abs(lk["sim"] - tau.astype(np.float64)[None, :]) < 1e-4).any()
+    assert int(mc.item()) == lk["miss_count"] > 0
+    rK, rV, rc = orc.fill_cache_buffer(srcK.numpy(), srcV.numpy(), got_idx, None, cbK.numpy(),
+                                       cbV.numpy(), lk["miss_list"])
+    assert rc == 0
+    assert np.array_equal(gK.cpu().numpy().view(np.uint16), rK)
+    assert np.array_equal(gV.cpu().numpy().view(np.uint16), rV)
+    ref, _ = orc.hybrid_attn(q.numpy(), rK, rV, got_idx, pK.numpy(), pV.numpy(), pid, scale_for())
+    assert_close(out.cpu().numpy(), ref, "retrieval + fill + attention")
