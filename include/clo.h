@@ -327,9 +327,10 @@ clo_status clo_hybrid_decode_attn(const clo_half* q, const clo_half* cbK,
  * Fig. 9: the next layer's lookup runs while the current layer computes; the
  * separate lookup launch of each layer is saved, CLO section 5's concern with
  * launch overhead).  The results are those of the two calls made separately
- * (the lookup reads nothing the attention writes).  The lookup is carried by
- * the attention's merge launch as one extra 8-CTA cluster and starts while the
- * main attention kernel drains.
+ * (the lookup reads nothing the attention writes).  The lookup runs as one
+ * 8-CTA cluster while the main attention kernel drains: for up to 64
+ * (batch row, KV head) groups inside the attention's merge launch, for more in
+ * a launch of its own right after the main kernel.
  * Arguments up to err_flag: as clo_hybrid_decode_attn.  q_next .. miss_count_next:
  * as clo_lookup_update for the next layer (same B, Hq, Hkv, d).  opts: as for
  * clo_hybrid_decode_attn.

@@ -1248,8 +1248,8 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
         cudaSuccess)
         return CLO_ERR_CUDA;
     // The fill starts as soon as every main-kernel CTA has passed its
-    // dependency wait and runs beside them; the merge launch below waits for
-    // the fill, which waits for the main kernel at its end.
+    // dependency wait and runs beside them; the launches below wait for it,
+    // and it waits for the main kernel at its end.
     if (fill != nullptr &&
         launch_fill(*fill, static_cast<int>(fill_grid), true, stream) != cudaSuccess)
         return CLO_ERR_CUDA;
@@ -1264,6 +1264,14 @@ static clo_status launch_attention(const Geo& geo, AttnOut o, long long n_tiles_
         const long long most = geo.max_partials_host(C);
         const int ngrp_all = MERGE_THREADS / (o.G * MERGE_ITEMS);
         hpb = most <= static_cast<long long>(ngrp_all) * MERGE_UNROLL ? o.G : 1;
+    }
+    // A large lookup runs beside the main kernel's drain, launched after it
+    // (and after the fill, whose CTAs start first); the merge launch then
+    // carries nothing else.  A small one rides in the merge launch (below).
+    if (lookup != nullptr &&
+        static_cast<long long>(lookup->B) * lookup->Hkv >= LK_BESIDE_MIN_GROUPS) {
+        if (launch_lookup_beside(*lookup, stream) != cudaSuccess) return CLO_ERR_CUDA;
+        lookup = nullptr;
     }
     LookupParams none{};
     if (lookup == nullptr) {

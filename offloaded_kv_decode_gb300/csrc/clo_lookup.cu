@@ -49,6 +49,35 @@ __global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_WIDE_THR
     lookup_cluster<LK_WIDE_THREADS / 32>(p, miss_sm, &cta_misses);
 }
 
+// The lookup launched beside the kernel before it: a main kernel that lets
+// its dependents start only after its own dependency wait, and writes nothing
+// the lookup reads or writes.  Every kernel before that one has then
+// finished, so the lookup reads its inputs at once; it waits for that kernel
+// at its end, so a kernel launched after the lookup still finds both
+// finished.  16-warp CTAs held to 64 registers a thread (32K registers, half
+// an SM's) fit on an SM once two attention CTAs there have finished, so a
+// large lookup runs in the main kernel's drain.  (8- and 4-warp CTAs, which
+// fit earlier but score several groups a warp, measured slower: Qwen2.5-14B
+// batch-16 step 142.1 / 141.1 / 135.8 us a layer-step with 4 / 8 / 16 warps.)
+constexpr int LK_BESIDE_THREADS = 512;
+
+__global__ void __cluster_dims__(LK_CLUSTER, 1, 1) __launch_bounds__(LK_BESIDE_THREADS, 2)
+    lookup_beside_kernel(const LookupParams p) {
+    extern __shared__ uint8_t miss_sm[];
+    __shared__ int cta_misses;
+    pdl_launch_dependents();
+    lookup_cluster<LK_BESIDE_THREADS / 32>(p, miss_sm, &cta_misses);
+    pdl_wait();
+}
+
+cudaError_t launch_lookup_beside(const LookupParams& p, cudaStream_t stream) {
+    const int per_cta = lookup_smem_bytes(p.B, p.Hkv);
+    if (!prepare_kernel(reinterpret_cast<const void*>(lookup_beside_kernel), per_cta))
+        return cudaErrorUnknown;
+    return launch_pdl(lookup_beside_kernel, dim3(LK_CLUSTER), dim3(LK_BESIDE_THREADS),
+                      static_cast<size_t>(per_cta), stream, p);
+}
+
 }  // namespace clo
 
 using namespace clo;

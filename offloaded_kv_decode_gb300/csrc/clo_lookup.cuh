@@ -1,7 +1,8 @@
 // clo_lookup.cuh -- the head-wise approximate-cache lookup + query-label update
 // (CLO section 2, Eq. 10, section 3 Fig. 7) as a device routine run by one
-// thread-block cluster, shared by the stand-alone lookup kernel and by the
-// attention's merge kernel when the next layer's lookup rides in its launch.
+// thread-block cluster, shared by the stand-alone lookup kernel, by the
+// attention's merge kernel when a small next-layer lookup rides in its launch,
+// and by the lookup launched beside the attention's main kernel.
 //
 // One cluster of LK_CLUSTER CTAs covers all (batch row, KV head) groups: each
 // CTA takes a contiguous share and one warp scores one group; every lane holds
@@ -174,5 +175,20 @@ inline clo_status make_lookup_params(const clo_half* q, clo_half* labels, const 
 
 // Shared-memory bytes lookup_cluster needs a CTA for B*Hkv groups.
 inline int lookup_smem_bytes(int B, int Hkv) { return (B * Hkv + LK_CLUSTER - 1) / LK_CLUSTER; }
+
+// Launches the lookup as one cluster directly after a libclo main kernel,
+// beside it (see lookup_beside_kernel in clo_lookup.cu).
+cudaError_t launch_lookup_beside(const LookupParams& p, cudaStream_t stream);
+
+// A lookup of at least this many (batch row, KV head) groups is carried beside
+// the attention's main kernel; a smaller one rides in the attention's merge
+// launch.  A launch of
+// its own adds a step to the chain, which a small lookup does not repay (per
+// layer-step, one box: the B1 128K step with 8 groups 32.7 us in the merge
+// launch, 36.2 us beside; the B8 32K layer with 64 groups 58.4 and 59.6 us),
+// while a large one, left to run after the drain, delays the next layer (the
+// Qwen2.5-14B batch-16 step with 128 groups: 138.5 us in the merge launch,
+// 135.8 us beside).
+constexpr int LK_BESIDE_MIN_GROUPS = 65;
 
 }  // namespace clo
