@@ -389,8 +389,9 @@ typedef struct clo_lookup_args {
  *     main kernel in CTA slots that grid leaves free: with opts->num_ctas == 0
  *     the attention takes the default grid less fill->num_ctas CTAs (less the
  *     fill's default share when that is 0);
- *   - lookup (may be NULL): clo_lookup_update for layer l+2, carried by the
- *     attention's merge launch as in clo_hybrid_decode_attn_lookup.
+ *   - lookup (may be NULL): clo_lookup_update for layer l+2, carried as in
+ *     clo_hybrid_decode_attn_lookup (in the attention's merge launch, or for
+ *     more than 64 groups in a launch of its own after the fill).
  * Called for l = 0, 1, ... this gives each layer's lookup one layer of
  * compute ahead of the layer's attention, and its fill the whole attention of
  * the layer before.  The results are those of the three calls made
