@@ -194,6 +194,9 @@ MISS_CASES = [
     ("b20_wide", dict(B=20, Hq=32, Hkv=8, T=200, Np=2), "all_one", 0),
     ("b64_gqa8", dict(B=64, Hq=64, Hkv=8, T=64, Np=1), "half_one", 37),
     ("mha_b5", dict(B=5, Hq=16, Hkv=16, T=300, Np=3), "all_one", 0),
+    # 96 groups: the lookup runs in a launch of its own beside the main kernel,
+    # and with one attention CTA no merge launch follows it.
+    ("b12_beside_one_cta", dict(B=12, Hq=32, Hkv=8, T=300, Np=2), "half_one", 1),
 ]
 
 
