@@ -63,6 +63,12 @@ HALF = 2
 
 # ---------------------------------------------------------------- byte accounting
 
+# A lookup carried by an attention call rides in its merge launch for up to
+# this many (batch row, KV head) groups, else in a launch of its own
+# (clo_hybrid_decode_attn_lookup, include/clo.h).
+LOOKUP_IN_MERGE_MAX_GROUPS = 64
+
+
 def hybrid_attn_bytes(cfg) -> int:
     """Algorithmic bytes of one hybrid attention launch (one layer): the
     selected Cache Buffer rows and the full persistent rows (K and V), the
@@ -285,8 +291,13 @@ class HybridWorkload:
 
     def launches_per_step(self) -> int:
         extra = (1 if self.restore is not None else 0) + (self.L if self.cfg.miss_fill else 0)
-        if self.schedule in ("fused", "pipelined"):  # main kernel + merge launch (+ lookup)
-            return 1 + self.L * 2 + extra
+        if self.schedule in ("fused", "pipelined"):
+            # The main kernel; the carried lookup, in the merge launch or, for
+            # more than 64 groups, in a launch of its own (include/clo.h); the
+            # merge launch where there are partials to merge.
+            beside = self.cfg.B * self.cfg.Hkv > LOOKUP_IN_MERGE_MAX_GROUPS
+            per_layer = 1 + (1 if beside else 0) + (1 if self.attn_kernels == 2 or not beside else 0)
+            return 1 + self.L * per_layer + extra
         return 1 + self.L * (1 + self.attn_kernels) + extra
 
     def _fill(self, step: int, l: int, events=None):
