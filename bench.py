@@ -375,7 +375,7 @@ class HybridWorkload:
         for it.  With the "pipelined" schedule every layer is one
         clo_hybrid_decode_layer call on one stream: the attention of layer l,
         the fill of layer l+1 beside it (its CTAs in slots the attention grid
-        leaves free) and the lookup of layer l+2 in its merge launch, so each
+        leaves free) and the lookup of layer l+2 carried after it, so each
         layer's lookup runs a layer of compute ahead of the attention before
         it, and its fill beside that attention (CLO section 3 Fig. 9); the
         step's last two calls fill and look up the next step's first layers.
@@ -615,8 +615,8 @@ class HybridWorkload:
                                "fill on a second stream beside this layer's attention",
                     "serial": "before each layer's attention, same stream",
                     "pipelined": "one call a layer on one stream: attention l, the miss-path "
-                                 "fill of layer l+1 beside it, the lookup of layer l+2 in its "
-                                 "merge launch"}[self.schedule],
+                                 "fill of layer l+1 beside it, the lookup of layer l+2 carried "
+                                 "after it"}[self.schedule],
                 "attention_ctas": self.main_ctas or "one full wave",
                 "physical_buffer_sets": self.n_inst,
                 "l2": f"inputs larger than L2: a buffer is re-read after "
@@ -1473,8 +1473,8 @@ def main(argv=None):
                          "layer's lookup on the main stream, then its miss-path fill on a second "
                          "stream beside this layer's attention; pipelined: one "
                          "clo_hybrid_decode_layer call a layer on one stream (attention l, the "
-                         "fill of layer l+1 beside it, the lookup of layer l+2 in its merge "
-                         "launch)")
+                         "fill of layer l+1 beside it, the lookup of layer l+2 carried after "
+                         "it)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--side-ctas", type=int, default=None,
